@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Throughput of the ZeRO step on GB300: parameters updated per second and
+achieved HBM bandwidth, through the library's C ABI.
+
+A step is one pass of the whole hot path over one batch of synthetic
+gradients: the mean reduce-scatter of W ranks' 16-bit gradients, Adam with
+bias correction on the fp32 master / m / v, the recast and gather of the
+16-bit working copy and, for ZeRO-3, the per-unit gather / release /
+re-gather schedule.  The default workload is the ZeRO-3 one (24 transformer-
+layer units of 50,331,648 parameters, 8 simulated ranks, bf16), the only one
+that passes through every stage; ``--workload`` selects the GPT-2-small
+(ZeRO-2) or GPT-2-1.5B (ZeRO-1) flat vectors instead.
+
+Prints one JSON line.  ``value`` is whole-job parameters per second with the
+inputs resident in HBM; ``e2e`` is the same metric with the gradients copied
+in from pinned host memory and the 16-bit working copy read back every step;
+``roofline`` is for the fused reduce-scatter + Adam + recast kernel, timed
+per launch with CUDA events on its own stream inside the timed region;
+``cpu_baseline`` is the CPU oracle timed on a bounded sample on this host.
+
+``--impl reference`` times the CPU oracle instead (on the host cores, a
+bounded sample per step) and prints the same line with ``"impl": "reference"``.
+
+Several GPUs (``--gpus N`` under torchrun) run N independent replicas of the
+single-GPU step: the method's ranks are simulated inside one GPU, so there is
+no data-path collective; a barrier and a max over ranks bracket the timing.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "params updated/sec per ZeRO step and achieved HBM GB/s vs GB300 peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="zero3_24x50m_w8",
+                   choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1"])
+    p.add_argument("--dtype", choices=["bf16", "fp16"], default=None)
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
+    return p.parse_args(argv)
+
+
+# ---- workload arithmetic ----------------------------------------------------------
+
+def workload(name):
+    import workloads as wk
+    return wk.WORKLOADS[name]
+
+
+def scheme_of(wl):
+    return wl.schemes[0]
+
+
+def layout_sizes(wl):
+    """(n_pad, unit elements per fused launch, units) of the flat layout."""
+    W = wl.W
+    units = wl.units() if scheme_of(wl) == 3 else [wl.n]
+    padded = [-(-u // W) * W for u in units]
+    return sum(padded), padded, units
+
+
+def algorithmic_bytes(wl):
+    """Bytes a step must move: the fused pass reads 2 W + 12 and writes 14
+    bytes per element; each ZeRO-3 gather reads and writes 2 bytes per
+    element, twice per step."""
+    n_pad, _, _ = layout_sizes(wl)
+    fused = (2 * wl.W + 26) * n_pad
+    gathers = 8 * n_pad if scheme_of(wl) == 3 else 0
+    return fused, gathers
+
+
+# ---- environment facts -------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel_file: str, workload_name: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"fused_step_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m1 = re.search(r"traffic_bytes_per_launch\s*=\s*(\d+)", text)
+    m2 = re.search(r"kernel_source_sha256\s*=\s*([0-9a-f]{64})", text)
+    if not (m1 and m2):
+        return None
+    src = open(os.path.join(ROOT, "zero_sharded_mixed_step_gb300", "csrc", kernel_file), "rb").read()
+    if hashlib.sha256(src).hexdigest() != m2.group(1):
+        return None
+    return int(m1.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id, self.proc, self.lines = gpu_id, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the CPU oracle (the CPU baseline leg and the reference arm) --------------------
+
+def oracle_sample_step_seconds(wl, sample_elems: int, dtype: str):
+    """Seconds the oracle takes for one step of ``wl`` restricted to a sample
+    of about ``sample_elems`` parameters (ZeRO-3: whole units shrunk to that
+    size; otherwise the first sample_elems parameters), on synthetic draws."""
+    import numpy as np
+    import workloads as wk
+    from oracle import zero_oracle as z
+    scheme = scheme_of(wl)
+    W = wl.W
+    sample_elems = max(W, sample_elems // W * W)
+    units = [sample_elems] if scheme != 3 else [min(sample_elems, wl.units()[0])]
+    small = wk.scaled(wl, unit_sizes=units, name=wl.name + "_sample") if scheme == 3 else \
+        wk.scaled(wl, n=sample_elems, name=wl.name + "_sample")
+    theta0 = wk.draw_theta0(small, "cpu").numpy()
+    draws = [wk.to_numpy16(g) for g in wk.GradSource(small, dtype, "cpu").step(1)]
+    orc = z.make_scheme(scheme, W, theta0, dtype, units if scheme == 3 else None)
+    grads = [z.place(g, orc.layout) for g in draws]
+    t0 = time.perf_counter()
+    orc.step(grads, wl.lr, wl.beta1, wl.beta2, wl.eps)
+    dt = time.perf_counter() - t0
+    return dt, small.n
+
+
+def cpu_cores_note():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        m = re.search(r"Model name:\s*(.+)", out)
+        model = m.group(1).strip() if m else ""
+    except Exception:
+        pass
+    return n, model
+
+
+def calibrate_sample(wl, dtype, budget_s):
+    """Sample size whose oracle step takes about budget_s seconds."""
+    dt, n = oracle_sample_step_seconds(wl, 1 << 20, dtype)
+    per = dt / n
+    return int(max(1 << 18, min(budget_s / per, wl.n)))
+
+
+def cpu_baseline(wl, dtype, budget_s):
+    size = calibrate_sample(wl, dtype, budget_s)
+    dt, n = oracle_sample_step_seconds(wl, size, dtype)
+    host_cores, model = cpu_cores_note()
+    what = (f"one step (t=1) of the oracle on {n:,} of the {wl.n:,} parameters "
+            + ("(one unit shrunk to that size, full ZeRO-3 schedule)" if scheme_of(wl) == 3 else "(leading slice)")
+            + f", W={wl.W}, {dtype} gradients; NumPy elementwise, one thread of {host_cores} host cores"
+            + (f" ({model})" if model else ""))
+    return {"value": n / dt, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": what,
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = workload(args.workload)
+    dtype = args.dtype or wl.dtypes[0]
+    budget = max(0.2, 150.0 / max(1, args.steps + args.warmup))
+    size = calibrate_sample(wl, dtype, budget)
+    for _ in range(args.warmup):
+        oracle_sample_step_seconds(wl, size, dtype)
+    total, elems = 0.0, 0
+    for _ in range(args.steps):
+        dt, n = oracle_sample_step_seconds(wl, size, dtype)
+        total += dt
+        elems += n
+    value = elems / total
+    host_cores, model = cpu_cores_note()
+    n_pad, per_launch, units = layout_sizes(wl)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, dtype, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the oracle on {elems // args.steps:,} of {wl.n:,} parameters, "
+                                   f"one NumPy thread of {host_cores} host cores ({model})"},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(wl, dtype, gpus):
+    n_pad, per_launch, units = layout_sizes(wl)
+    fused, gathers = algorithmic_bytes(wl)
+    names = {0: "data parallel", 1: "ZeRO-1", 2: "ZeRO-2", 3: "ZeRO-3"}
+    return {"workload": wl.name, "scheme": names[scheme_of(wl)], "W": wl.W, "params": wl.n, "padded": n_pad,
+            "units": len(units), "grad_dtype": dtype, "work_dtype": dtype, "master_dtype": "f32",
+            "algorithmic_bytes_per_step": fused + gathers,
+            "l2": f"inputs larger than L2: {(fused + gathers) / 1e9:.1f} GB touched per step vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB of L2",
+            "parallelism": "simulated DP ranks in one GPU" + (f"; {gpus} independent replicas" if gpus > 1 else "")}
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from zero_sharded_mixed_step_gb300 import build
+    build.build()
+    import zero_sharded_mixed_step_gb300 as zs
+    import workloads as wk
+
+    wl = workload(args.workload)
+    dtype = args.dtype or wl.dtypes[0]
+    scheme = scheme_of(wl)
+    n_pad, per_launch, units = layout_sizes(wl)
+    su = torch.cuda.Stream(dev)
+    sg = torch.cuda.Stream(dev) if scheme == 3 else None
+    with torch.cuda.stream(su):
+        theta0 = wk.draw_theta0(wl, dev)
+        step = zs.ZeroStep(scheme, wl.W, units, dtype, theta0=theta0, device=dev, stream=su, gather_stream=sg,
+                           with_grad_buffers=True)
+        del theta0
+        for r, d in enumerate(wk.GradSource(wl, dtype, dev).step(1)):
+            step.place_(step.grads[r], d)
+            del d
+    torch.cuda.synchronize()
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step.step(step.grads, *hp, t)
+    torch.cuda.synchronize()
+
+    # ---- timed region: inputs resident in HBM --------------------------------------
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_FUSED)
+    zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_GATHER)
+    zs.zero_enable_timing(step.ctx, True)
+    launches0 = step.stat(zs.ZERO_STAT_LAUNCHES)
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clocks:
+        e0.record(su)
+        for _ in range(args.steps):
+            t += 1
+            step.step(step.grads, *hp, t)
+        e1.record(su)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    launches = step.stat(zs.ZERO_STAT_LAUNCHES) - launches0
+    zs.zero_enable_timing(step.ctx, False)
+    fused_ms, fused_n = zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_FUSED)
+    gather_ms, gather_n = zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_GATHER)
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = world * wl.n * args.steps / (ms / 1e3)
+    fused_b, gather_b = algorithmic_bytes(wl)
+    step_gbs = (fused_b + gather_b) / (ms_per_step / 1e3) / 1e9
+
+    # roofline of the dominant kernel: the fused pass, per launch
+    peak, peak_src = hbm_peak()
+    per_launch_bytes = (2 * wl.W + 26) * per_launch[0]
+    fused_avg_ms = fused_ms / max(1, fused_n)
+    achieved = per_launch_bytes / (fused_avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": recorded_traffic("fused_step.cu", wl.name), "kernel": "fused_step_vector",
+                "peak_source": f"{peak_src} copy bandwidth", "launch_ms": fused_avg_ms,
+                "algorithmic_bytes_per_launch": per_launch_bytes, "frac_of_8tbs_nominal": achieved / 8000.0}
+    gather_info = None
+    if gather_n:
+        gb = 4 * per_launch[0]
+        gather_info = {"launch_ms": gather_ms / gather_n, "achieved_gbs": gb / (gather_ms / gather_n / 1e3) / 1e9,
+                       "launches": gather_n}
+
+    # ---- end to end: gradients from pinned host memory, working copy read back ------
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        host_grads = [g.to("cpu").pin_memory() for g in step.grads]
+        if scheme == 3:
+            dev_out = step.shard16
+        else:
+            dev_out = [step.p16]
+        host_out = [torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in dev_out]
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        h0 = time.perf_counter()
+        with torch.cuda.stream(su):
+            for _ in range(args.e2e_steps):
+                t += 1
+                for d, h in zip(step.grads, host_grads):
+                    d.copy_(h, non_blocking=True)
+                step.step(step.grads, *hp, t)
+                for h, d in zip(host_out, dev_out):
+                    h.copy_(d, non_blocking=True)
+                su.synchronize()
+        e2e_s = time.perf_counter() - h0
+        if world > 1:
+            tt = torch.tensor([e2e_s], dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        h2d = sum(h.numel() * h.element_size() for h in host_grads)
+        d2h = sum(h.numel() * h.element_size() for h in host_out)
+        e2e = {"value": world * wl.n * args.e2e_steps / e2e_s, "unit": "params/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
+               "path": "pinned host gradients -> cudaMemcpyAsync -> zero_step -> working copy -> pinned host"}
+        del host_grads, host_out
+
+    step.close()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, dtype, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_of(wl, dtype, world),
+            "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
+            "roofline": roofline, "gather": gather_info, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

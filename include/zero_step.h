@@ -1,0 +1,303 @@
+/*
+ * zero_step.h - C ABI of libzero_gb300.so, the ZeRO step on one GB300.
+ *
+ * The data-parallel hot path of ZeRO over a flat parameter vector, for W
+ * data-parallel ranks simulated inside one GPU's memory:
+ *
+ *   (1) reduce-scatter: the mean over the W ranks of their 16-bit gradients,
+ *       summed in rank order, for every element of each rank's 1/W shard;
+ *   (2) Adam with bias correction on that shard's fp32 master, m and v;
+ *   (3) the round-to-nearest-even recast of the master to the 16-bit working
+ *       copy, written straight to its place in the full vector (the
+ *       all-gather) or, for ZeRO-3, into the owning rank's 16-bit shard;
+ *   (4) for ZeRO-3, the per-unit gather / release / re-gather schedule.
+ *
+ * Sources (page title and section):
+ *   "The four schemes" (Zero From Scratch lab): the three flags that define
+ *     data parallel and ZeRO-1/2/3, the per-shard Adam update, the step of
+ *     each scheme, the resident and peak accounting.
+ *   "ZeRO and FSDP" (AI infra handbook): the closed forms 16 Psi,
+ *     4 Psi + 12 Psi/N, 2 Psi + 14 Psi/N, 16 Psi/N; the zero-padded even
+ *     split of the flat vector; the per-unit ZeRO-3 flow with prefetch.
+ *   "ZeRO, annotated" sections 5 and 7, "One Poem Suffices: ZeRO" section
+ *     4.1.4 and appendix B, "Sharding the States": traffic per rank under
+ *     ring collectives, (N-1)/N of the data per collective.
+ *
+ * Layout.  n real parameters are split into units (one unit for data
+ * parallel, ZeRO-1 and ZeRO-2; the caller's units, e.g. one per transformer
+ * layer, for ZeRO-3).  Unit u holds unit_sizes[u] parameters padded with
+ * zeros to S_u * W elements, S_u = ceil(unit_sizes[u] / W); units follow one
+ * another in a flat vector of n_pad = sum_u S_u * W elements.  Rank r owns
+ * [off_u + r S_u, off_u + (r + 1) S_u) of unit u.  The fp32 master, m and v
+ * are n_pad floats each in this flat order; every rank's gradient vector is
+ * n_pad 16-bit values in the same order (zeros in the padding).
+ *
+ * Memory ownership.  The caller allocates and owns every device buffer and
+ * every stream; the library keeps non-owning pointers and calls no device
+ * allocator.  master, m and v must be 32-byte aligned, every other device
+ * pointer 16-byte aligned (ZERO_E_ALIGN otherwise).
+ *
+ * Errors.  Every function that returns int returns ZERO_OK (0) or a negative
+ * ZERO_E_* code; functions returning int64_t return a negative code on error.
+ * zero_last_error() gives a message for the calling thread's last error.
+ * Arguments are checked on the host before anything is launched: a call that
+ * fails a check has enqueued no GPU work.
+ *
+ * Asynchrony.  zero_step, zero_gather_unit, zero_update_unit and
+ * zero_refresh_working_copy enqueue work on the context's streams and return
+ * without waiting; zero_sync waits (with a deadline), and zero_get_state /
+ * zero_set_state wait for their own copies.
+ */
+#ifndef ZERO_STEP_H
+#define ZERO_STEP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define ZERO_OK          0
+#define ZERO_E_ARG      -1  /* an argument is out of range or inconsistent      */
+#define ZERO_E_ALIGN    -2  /* a device pointer is not 16-byte aligned           */
+#define ZERO_E_CUDA     -3  /* a CUDA runtime call failed                        */
+#define ZERO_E_RANK     -4  /* a simulated rank is marked unavailable            */
+#define ZERO_E_TIMEOUT  -5  /* zero_sync's deadline passed before the work ended */
+#define ZERO_E_STATE    -6  /* call out of order (step counter, unit not live)   */
+
+/* ---- schemes ("The four schemes": shard_opt / shard_grad / shard_param) - */
+#define ZERO_SCHEME_DP  0   /* nothing sharded, gradients all-reduced           */
+#define ZERO_SCHEME_Z1  1   /* optimizer state sharded                          */
+#define ZERO_SCHEME_Z2  2   /* + gradients sharded                              */
+#define ZERO_SCHEME_Z3  3   /* + 16-bit parameters sharded, gathered per unit   */
+
+/* ---- 16-bit formats ---------------------------------------------------- */
+#define ZERO_FP16       0
+#define ZERO_BF16       1
+
+/* ---- accounting kinds --------------------------------------------------- */
+#define ZERO_RESIDENT   0
+#define ZERO_PEAK       1
+
+/* ---- kernel variants for the fused reduce + Adam + cast pass ------------ */
+#define ZERO_VARIANT_AUTO   0  /* the fastest measured variant                    */
+#define ZERO_VARIANT_VECTOR 1  /* 256-bit vector loads into registers             */
+
+/* ---- statistics (zero_stat) --------------------------------------------- */
+#define ZERO_STAT_COMM_BYTES      0  /* bytes a rank would send, cumulative       */
+#define ZERO_STAT_LAUNCHES        1  /* kernels this context launched, cumulative */
+#define ZERO_STAT_GATHERS         2  /* unit all-gathers performed                */
+#define ZERO_STAT_SCATTERS        3  /* unit reduce-scatters performed            */
+#define ZERO_STAT_LIVE_ELEMS      4  /* gathered 16-bit elements live right now   */
+#define ZERO_STAT_PEAK_LIVE_ELEMS 5  /* most gathered elements ever live at once  */
+#define ZERO_STAT_T               6  /* the last step counter used                */
+#define ZERO_STAT_DEVICE_ERRORS   7  /* bounded waits that gave up (see variants) */
+
+typedef struct zero_ctx zero_ctx;
+
+/*
+ * Host hook for ZeRO-3 steps.  zero_step calls it on the host once per
+ * gathered unit, after the unit's gather has been enqueued and before the
+ * unit is released: phase 0 is the forward pass, 1 the backward pass.
+ * unit_buf holds the unit's S_u * W 16-bit values in flat order; work that
+ * reads it must be enqueued on `stream` (a cudaStream_t) and must not keep
+ * the pointer: the buffer is reused for a later unit once that work ends.
+ */
+typedef void (*zero_unit_hook)(void* user, int phase, int64_t unit, void* unit_buf, void* stream);
+
+/* ---- pure host queries (no GPU needed) --------------------------------- */
+
+/*
+ * Buffer sizes for a configuration.  out[0] = n, out[1] = n_pad (floats in
+ * each of master / m / v, 16-bit values in each rank's gradient vector),
+ * out[2] = elements of the full 16-bit working copy (n_pad for DP/Z1/Z2,
+ * 0 for Z3), out[3] = elements of each rank's 16-bit shard store (Z3:
+ * sum_u S_u; else 0), out[4] = elements of one ZeRO-3 unit buffer
+ * (max_u S_u * W; else 0), out[5] = number of units.  DP/Z1/Z2 take exactly
+ * one unit (unit_sizes[0] = n).  Returns ZERO_E_ARG for W outside
+ * [1, ZERO_MAX_RANKS], no units, or a negative unit size.
+ */
+#define ZERO_MAX_RANKS 64
+int zero_buffer_sizes(int scheme, int W, int64_t n_units, const int64_t* unit_sizes, int64_t* out);
+
+/*
+ * Per-unit layout: off[u] (flat offset of unit u), shard[u] (S_u) and
+ * off16[u] (offset of unit u's shard inside each rank's shard store), for
+ * u < n_units.  Any of the three output arrays may be NULL.
+ */
+int zero_layout(int W, int64_t n_units, const int64_t* unit_sizes, int64_t* off, int64_t* shard, int64_t* off16);
+
+/*
+ * Model-state bytes per rank ("ZeRO and FSDP", the three stages; "The four
+ * schemes", bytes_per_param): resident = 16 n (DP), 4 n + 12 S (Z1),
+ * 2 n + 14 S (Z2), 16 S (Z3) with S = ceil(n / W).  kind ZERO_PEAK adds,
+ * for ZeRO-3 only, 2 bytes for each of `gathered_elems` gathered 16-bit
+ * values live at once.  Negative on a bad argument.
+ */
+int64_t zero_bytes_per_rank(int scheme, int64_t n, int W, int kind, int64_t gathered_elems);
+
+/*
+ * Bytes one rank sends per step under ring collectives of 2-byte values
+ * ("Sharding the States": (n-1)/n of 4 N, and of 6 N for stage 3):
+ * 2 (W-1) S 2 for DP/Z1/Z2 and 3 (W-1) S 2 for ZeRO-3, S = ceil(n / W).
+ */
+int64_t zero_comm_bytes_closed_form(int scheme, int64_t n, int W);
+
+/* ---- context lifetime --------------------------------------------------- */
+
+/*
+ * Create a context.  No GPU work and no CUDA call happen here.
+ *   scheme            ZERO_SCHEME_*.
+ *   W                 simulated ranks, 1..ZERO_MAX_RANKS.
+ *   n                 real parameters, = sum of unit_sizes.
+ *   n_units, unit_sizes  the units (exactly one for DP/Z1/Z2).
+ *   grad_dtype, work_dtype  ZERO_FP16 or ZERO_BF16: the gradients' format and
+ *                     the 16-bit working copy's format.
+ *   master, m, v      device, n_pad floats each, flat layout.  The caller
+ *                     writes theta0 into master (zeros in the padding) and
+ *                     zeros into m and v before the first step.
+ *   p16               device, n_pad 16-bit values: the full working copy
+ *                     (DP/Z1/Z2; must be NULL for Z3).
+ *   shard16           host array of W device pointers, each rank's shard
+ *                     store of sum_u S_u values (Z3; NULL otherwise).
+ *   unit_bufs         host array of 2 device pointers, each max_u S_u * W
+ *                     16-bit values: the ping-pong gather buffers zero_step
+ *                     uses for ZeRO-3 (Z3; NULL otherwise).
+ *   stream_update     cudaStream_t for updates (may be the caller's stream;
+ *                     NULL means the legacy default stream).
+ *   stream_gather     cudaStream_t for ZeRO-3 gathers, so that the next
+ *                     unit's gather overlaps the current update; NULL means
+ *                     stream_update (no overlap).
+ * On success *out receives the context.  Call zero_refresh_working_copy
+ * once after writing theta0, before the first step or gather.
+ */
+int zero_init(zero_ctx** out, int scheme, int W, int64_t n, int64_t n_units, const int64_t* unit_sizes,
+              int grad_dtype, int work_dtype, float* master, float* m, float* v, void* p16,
+              void* const* shard16, void* const* unit_bufs, void* stream_update, void* stream_gather);
+
+/* Destroy a context (waits for its work first).  NULL is accepted. */
+int zero_destroy(zero_ctx* ctx);
+
+/* ---- the step ------------------------------------------------------------ */
+
+/*
+ * Cast the fp32 master to the 16-bit working copy (DP/Z1/Z2: p16; Z3: each
+ * rank's shard store), round to nearest even, on stream_update.
+ */
+int zero_refresh_working_copy(zero_ctx* ctx);
+
+/*
+ * One ZeRO step ("The four schemes": the step of each scheme).
+ *   scheme, W, n      must equal the context's (else ZERO_E_ARG).
+ *   grads             host array of W device pointers; rank w's gradients,
+ *                     n_pad values of grad_dtype in flat order, read only.
+ *   lr, beta1, beta2, eps  Adam hyper-parameters (0 <= beta < 1, eps > 0).
+ *   t                 the step counter, 1-based: must be the context's last
+ *                     step counter + 1 (ZERO_E_STATE otherwise).
+ * DP/Z1/Z2: one fused pass over the flat vector: mean of the W gradients,
+ * Adam, recast into p16.  Traffic counted: 2 (W-1) S 2 bytes.
+ * Z3: for u = 0..U-1 gather u (stream_gather), call the hook, release; then
+ * for u = U-1..0 gather u, call the hook, update unit u (stream_update),
+ * release.  The gather of the next unit overlaps the current unit's update;
+ * at most two unit buffers are live.  Traffic: 3 (W-1) S_u 2 bytes per unit.
+ * The step is ordered after earlier work on stream_update and all its work
+ * is finished when work enqueued later on stream_update starts.
+ */
+int zero_step(zero_ctx* ctx, int scheme, int W, int64_t n, const void* const* grads,
+              double lr, double beta1, double beta2, double eps, int64_t t);
+
+/* Register (fn != NULL) or clear the ZeRO-3 unit hook. */
+int zero_set_unit_hook(zero_ctx* ctx, zero_unit_hook fn, void* user);
+
+/* ---- ZeRO-3 driven by the caller ---------------------------------------- */
+
+/*
+ * Gather unit `unit` of a ZeRO-3 context: dst (device, S_u * W 16-bit values
+ * of work_dtype) receives every rank's shard of the unit in flat order, on
+ * `stream` (NULL: stream_gather).  The unit becomes live; gathering a live
+ * unit is ZERO_E_STATE.  Traffic counted: (W-1) S_u 2 bytes.
+ */
+int zero_gather_unit(zero_ctx* ctx, int64_t unit, void* dst, void* stream);
+
+/* Release a live unit (host bookkeeping; the buffer stays the caller's). */
+int zero_release_unit(zero_ctx* ctx, int64_t unit);
+
+/*
+ * Reduce-scatter + Adam + recast of one ZeRO-3 unit, on `stream` (NULL:
+ * stream_update).  grads as in zero_step.  t must be the context's step
+ * counter (another unit of the same step) or that + 1 (a new step).
+ * Traffic counted: (W-1) S_u 2 bytes.
+ */
+int zero_update_unit(zero_ctx* ctx, int64_t unit, const void* const* grads,
+                     double lr, double beta1, double beta2, double eps, int64_t t, void* stream);
+
+/* ---- state, statistics, waiting ------------------------------------------ */
+
+/*
+ * Copy master, m and v (n_pad floats each) out to the caller's buffers
+ * (host or device; any of them may be NULL) and the step counter to *t;
+ * waits for the copies.
+ */
+int zero_get_state(zero_ctx* ctx, float* master, float* m, float* v, int64_t* t);
+
+/*
+ * Copy master, m and v (n_pad floats each, host or device) into the
+ * context's buffers, set the step counter to t (>= 0), and refresh the
+ * 16-bit working copy; waits for the copies.
+ */
+int zero_set_state(zero_ctx* ctx, const float* master, const float* m, const float* v, int64_t t);
+
+/* Cumulative bytes one rank would have sent for the collectives run so far. */
+int64_t zero_comm_bytes_per_rank(const zero_ctx* ctx);
+
+/* One of the ZERO_STAT_* counters; negative on a bad argument. */
+int64_t zero_stat(const zero_ctx* ctx, int which);
+
+/*
+ * Wait until all work the context has enqueued has finished, polling with a
+ * host deadline of timeout_ms (< 0: no deadline).  ZERO_E_TIMEOUT when the
+ * deadline passes first; the work is left running and a later call may
+ * wait again.  ZERO_E_CUDA if the work failed; ZERO_E_STATE if a bounded
+ * device-side wait gave up (ZERO_STAT_DEVICE_ERRORS).
+ */
+int zero_sync(zero_ctx* ctx, int timeout_ms);
+
+/* ---- timing of the context's own kernels ---------------------------------- */
+#define ZERO_KERNEL_FUSED   0  /* the fused reduce-scatter + Adam + recast pass */
+#define ZERO_KERNEL_GATHER  1  /* ZeRO-3 unit gathers                           */
+#define ZERO_KERNEL_CAST    2  /* working-copy casts                            */
+
+/*
+ * Per-launch timing on (1) or off (0).  While on, every kernel the context
+ * launches is bracketed by two CUDA events recorded on the stream it is
+ * launched on; the events come from a pool the context owns.
+ */
+int zero_enable_timing(zero_ctx* ctx, int on);
+
+/*
+ * Wait for the timed launches of `kernel` (ZERO_KERNEL_*) recorded so far,
+ * return their summed device time in milliseconds and their number, and
+ * start a new tally for that kernel.  Either output may be NULL.
+ */
+int zero_read_timing(zero_ctx* ctx, int kernel, double* total_ms, int64_t* launches);
+
+/* Select the fused-pass variant (ZERO_VARIANT_*). */
+int zero_set_variant(zero_ctx* ctx, int variant);
+
+/*
+ * Host-side fault injection: mark simulated rank `rank` unavailable
+ * (available = 0) or back (1).  While any rank is unavailable, zero_step,
+ * zero_gather_unit and zero_update_unit return ZERO_E_RANK before launching
+ * anything, as a collective with a missing peer would fail.
+ */
+int zero_mark_rank(zero_ctx* ctx, int rank, int available);
+
+/* Message for the calling thread's last error ("" if none). */
+const char* zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_STEP_H */

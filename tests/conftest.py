@@ -8,3 +8,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (the sm_103a library on a GB300)")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def zlib():
+    """The C library, built in-tree if needed (nvcc cross-compiles without a GPU)."""
+    from zero_sharded_mixed_step_gb300 import build
+    build.build()
+    import zero_sharded_mixed_step_gb300 as zs
+    return zs.lib()

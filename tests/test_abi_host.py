@@ -1,0 +1,202 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+its accounting and layout equal the oracle's, and every argument check fails
+cleanly before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import zero_sharded_mixed_step_gb300 as zs
+from oracle import zero_oracle as z
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zero_step.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(zero_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(zlib):
+    names = declared_functions()
+    assert len(names) >= 20, names
+    for name in names:
+        assert hasattr(zlib, name), name
+    assert set(names) == set(zs.SIGNATURES), set(names) ^ set(zs.SIGNATURES)
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    consts = dict((k, int(v)) for k, v in re.findall(r"#define\s+(ZERO_[A-Z0-9_]+)\s+(-?\d+)", text))
+    for k, v in consts.items():
+        assert getattr(zs, k) == v, k
+
+
+@pytest.mark.parametrize("scheme", [0, 1, 2, 3])
+def test_bytes_per_rank_equals_oracle(zlib, scheme):
+    for n in (0, 1, 7, 8, 19210, 124_439_808, 1_557_611_200, 7_500_000_000, 1_000_000_000_000):
+        for W in (1, 2, 3, 4, 8, 16, 25, 64):
+            assert zs.zero_bytes_per_rank(scheme, n, W) == z.bytes_per_rank(scheme, n, W)
+            assert zs.zero_comm_bytes_closed_form(scheme, n, W) == z.comm_bytes_closed_form(scheme, n, W)
+            for g in (0, 5, 100_663_296):
+                assert zs.zero_bytes_per_rank(scheme, n, W, zs.ZERO_PEAK, g) == z.peak_bytes_per_rank(scheme, n, W, g)
+
+
+def test_accounting_pins_through_the_abi(zlib):
+    from tests.oracle_pins import load_accounting_pins
+    for row in load_accounting_pins():
+        if row["qty"] == "resident":
+            assert zs.zero_bytes_per_rank(row["scheme"], row["psi"], row["N"]) == row["exact"], row["id"]
+        if row["qty"] == "comm_bytes_step":
+            assert zs.zero_comm_bytes_closed_form(row["scheme"], row["psi"], row["N"]) == row["exact"], row["id"]
+    assert zs.zero_comm_bytes_closed_form(3, 24 * 50_331_648, 8) == 6_341_787_648
+
+
+@pytest.mark.parametrize("units,W", [([8], 4), ([37], 4), ([13, 24, 3], 4), ([50_331_648] * 24, 8),
+                                     ([1, 0, 5, 17], 8), ([1_557_611_200], 16), ([0], 3)])
+def test_layout_equals_oracle(zlib, units, W):
+    L = z.Layout(W, list(units))
+    off, shard, off16 = zs.zero_layout(W, units)
+    assert off == L.off and shard == L.S and off16 == L.off16
+    scheme = 3 if len(units) > 1 else 1
+    s = zs.zero_buffer_sizes(scheme, W, units)
+    assert s["n"] == L.n and s["n_pad"] == L.n_pad and s["units"] == len(units)
+    if scheme == 3:
+        assert s["shard_store"] == L.S_total and s["unit_buf"] == max(x * W for x in L.S) and s["p16"] == 0
+    else:
+        assert s["p16"] == L.n_pad and s["shard_store"] == 0
+
+
+def _err(fn, *args, **kw):
+    with pytest.raises(zs.ZeroError) as e:
+        fn(*args, **kw)
+    return e.value.code
+
+
+def test_bad_queries(zlib):
+    assert _err(zs.zero_buffer_sizes, 4, 8, [10]) == zs.ZERO_E_ARG
+    assert _err(zs.zero_buffer_sizes, 1, 0, [10]) == zs.ZERO_E_ARG
+    assert _err(zs.zero_buffer_sizes, 1, 65, [10]) == zs.ZERO_E_ARG
+    assert _err(zs.zero_buffer_sizes, 1, 8, [10, 10]) == zs.ZERO_E_ARG
+    assert _err(zs.zero_buffer_sizes, 3, 8, [10, -1]) == zs.ZERO_E_ARG
+    assert _err(zs.zero_buffer_sizes, 3, 8, []) == zs.ZERO_E_ARG
+    assert _err(zs.zero_bytes_per_rank, 1, -1, 8) == zs.ZERO_E_ARG
+    assert _err(zs.zero_bytes_per_rank, 1, 8, 0) == zs.ZERO_E_ARG
+    assert _err(zs.zero_bytes_per_rank, 1, 8, 4, 7) == zs.ZERO_E_ARG
+    assert _err(zs.zero_comm_bytes_closed_form, 9, 8, 4) == zs.ZERO_E_ARG
+    assert "scheme" in zs.zero_last_error()
+
+
+# Fake device addresses: zero_init makes no CUDA call, so no GPU is needed.
+A = 0x7F0000000000
+
+
+def fake(k):
+    return A + k * (1 << 30)
+
+
+def make_ctx(scheme=1, W=4, units=(37,), gdt=0, wdt=0):
+    n = sum(units)
+    if scheme == 3:
+        return zs.zero_init(scheme, W, n, list(units), gdt, wdt, fake(1), fake(2), fake(3), None,
+                            [fake(10 + r) for r in range(W)], [fake(8), fake(9)])
+    return zs.zero_init(scheme, W, n, list(units), gdt, wdt, fake(1), fake(2), fake(3), fake(4))
+
+
+def test_init_checks(zlib):
+    ok = make_ctx()
+    zs.zero_destroy(ok)
+    assert _err(zs.zero_init, 1, 0, 8, [8], 0, 0, fake(1), fake(2), fake(3), fake(4)) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 5, 4, 8, [8], 0, 0, fake(1), fake(2), fake(3), fake(4)) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 1, 4, 8, [8], 2, 0, fake(1), fake(2), fake(3), fake(4)) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 1, 4, 9, [8], 0, 0, fake(1), fake(2), fake(3), fake(4)) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 1, 4, 8, [8], 0, 0, None, fake(2), fake(3), fake(4)) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 1, 4, 8, [8], 0, 0, fake(1) + 4, fake(2), fake(3), fake(4)) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_init, 1, 4, 8, [8], 0, 0, fake(1), fake(2) + 16, fake(3), fake(4)) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_init, 1, 4, 8, [8], 0, 0, fake(1), fake(2), fake(3), fake(4) + 2) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_init, 1, 4, 8, [8], 0, 0, fake(1), fake(2), fake(3), None) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 1, 4, 8, [4, 4], 0, 0, fake(1), fake(2), fake(3), fake(4)) == zs.ZERO_E_ARG
+    # ZeRO-3 keeps no full copy, and needs its shard stores and two unit buffers
+    assert _err(zs.zero_init, 3, 2, 8, [8], 0, 0, fake(1), fake(2), fake(3), fake(4),
+                [fake(5), fake(6)], [fake(7), fake(8)]) == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 3, 2, 8, [8], 0, 0, fake(1), fake(2), fake(3), None, None, [fake(7), fake(8)]) \
+        == zs.ZERO_E_ARG
+    assert _err(zs.zero_init, 3, 2, 8, [8], 0, 0, fake(1), fake(2), fake(3), None,
+                [fake(5), fake(6) + 8], [fake(7), fake(8)]) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_init, 1, 2, 8, [8], 0, 0, fake(1), fake(2), fake(3), fake(4), [fake(5), fake(6)]) \
+        == zs.ZERO_E_ARG
+    zs.zero_destroy(None)
+
+
+def test_step_checks_before_any_launch(zlib):
+    c = make_ctx(scheme=2, W=4, units=(37,))
+    g = [fake(20 + r) for r in range(4)]
+    hp = (1e-3, 0.9, 0.999, 1e-8)
+    assert _err(zs.zero_step, c, 1, 4, 37, g, *hp, 1) == zs.ZERO_E_ARG          # scheme differs
+    assert _err(zs.zero_step, c, 2, 8, 37, g, *hp, 1) == zs.ZERO_E_ARG          # W differs
+    assert _err(zs.zero_step, c, 2, 4, 36, g, *hp, 1) == zs.ZERO_E_ARG          # n differs
+    assert _err(zs.zero_step, c, 2, 4, 37, g, *hp, 0) == zs.ZERO_E_STATE        # t starts at 1
+    assert _err(zs.zero_step, c, 2, 4, 37, g, *hp, 2) == zs.ZERO_E_STATE        # t must follow
+    assert _err(zs.zero_step, c, 2, 4, 37, g, -1.0, 0.9, 0.999, 1e-8, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step, c, 2, 4, 37, g, 1e-3, 1.0, 0.999, 1e-8, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step, c, 2, 4, 37, g, 1e-3, 0.9, -0.1, 1e-8, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step, c, 2, 4, 37, g, 1e-3, 0.9, 0.999, 0.0, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step, c, 2, 4, 37, g, float("nan"), 0.9, 0.999, 1e-8, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step, c, 2, 4, 37, g[:3] + [None], *hp, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step, c, 2, 4, 37, g[:3] + [fake(30) + 2], *hp, 1) == zs.ZERO_E_ALIGN
+    # a rank that stopped answering fails the collective before anything launches
+    zs.zero_mark_rank(c, 2, False)
+    assert _err(zs.zero_step, c, 2, 4, 37, g, *hp, 1) == zs.ZERO_E_RANK
+    assert "rank 2" in zs.zero_last_error()
+    assert _err(zs.zero_mark_rank, c, 4, False) == zs.ZERO_E_ARG
+    assert zs.zero_stat(c, zs.ZERO_STAT_LAUNCHES) == 0
+    assert zs.zero_stat(c, zs.ZERO_STAT_T) == 0
+    assert zs.zero_comm_bytes_per_rank(c) == 0
+    assert _err(zs.zero_stat, c, 99) == zs.ZERO_E_ARG
+    assert _err(zs.zero_set_variant, c, 7) == zs.ZERO_E_ARG
+    zs.zero_destroy(c)
+
+
+def test_unit_calls_checks(zlib):
+    c = make_ctx(scheme=3, W=4, units=(13, 24, 3))
+    g = [fake(20 + r) for r in range(4)]
+    assert _err(zs.zero_gather_unit, c, 3, fake(40)) == zs.ZERO_E_ARG          # no unit 3
+    assert _err(zs.zero_gather_unit, c, -1, fake(40)) == zs.ZERO_E_ARG
+    assert _err(zs.zero_gather_unit, c, 0, fake(40) + 2) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_gather_unit, c, 0, None) == zs.ZERO_E_ARG
+    assert _err(zs.zero_release_unit, c, 1) == zs.ZERO_E_STATE                 # not gathered
+    assert _err(zs.zero_update_unit, c, 0, g, 1e-3, 0.9, 0.999, 1e-8, 2) == zs.ZERO_E_STATE
+    zs.zero_mark_rank(c, 0, False)
+    assert _err(zs.zero_gather_unit, c, 0, fake(40)) == zs.ZERO_E_RANK
+    assert _err(zs.zero_update_unit, c, 0, g, 1e-3, 0.9, 0.999, 1e-8, 1) == zs.ZERO_E_RANK
+    assert zs.zero_stat(c, zs.ZERO_STAT_GATHERS) == 0 and zs.zero_stat(c, zs.ZERO_STAT_LAUNCHES) == 0
+    zs.zero_destroy(c)
+    d = make_ctx(scheme=1)
+    assert _err(zs.zero_gather_unit, d, 0, fake(40)) == zs.ZERO_E_ARG          # not ZeRO-3
+    assert _err(zs.zero_update_unit, d, 0, g, 1e-3, 0.9, 0.999, 1e-8, 1) == zs.ZERO_E_ARG
+    zs.zero_destroy(d)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(zs, "_lib", None)
+    monkeypatch.setattr(zs, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(zs.ZeroLibraryMissing):
+        zs.zero_bytes_per_rank(1, 8, 4)
+
+
+def test_last_error_is_per_thread(zlib):
+    import threading
+    _err(zs.zero_bytes_per_rank, 9, 8, 4)
+    seen = {}
+
+    def other():
+        seen["msg"] = zs.zero_last_error()
+
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen["msg"] == "" and "scheme" in zs.zero_last_error()
+    assert isinstance(ctypes.c_int64(zs.zero_comm_bytes_closed_form(0, 8, 4)).value, int)

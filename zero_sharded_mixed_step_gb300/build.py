@@ -1,0 +1,76 @@
+"""Build libzero_gb300.so in-tree for sm_103a with nvcc (no CMake).
+
+Translation units are compiled in parallel into ``_build/`` at the
+repository root and linked, with the CUDA runtime linked statically, into
+``zero_sharded_mixed_step_gb300/libzero_gb300.so``.  Run
+``python -m zero_sharded_mixed_step_gb300.build`` or call ``build()``.
+"""
+
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(ROOT, "_build")
+LIB = os.path.join(HERE, "libzero_gb300.so")
+SOURCES = ["zero_api.cpp", "fused_step.cu", "copy_cast.cu"]
+HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(INCLUDE, "zero_step.h")]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH") or "/usr/local/cuda"
+    path = os.path.join(home, "bin", "nvcc")
+    return path if os.path.exists(path) else "nvcc"
+
+
+def _flags(ptxas_verbose: bool):
+    f = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    if ptxas_verbose:
+        f += ["-Xptxas", "-v"]
+    return f
+
+
+def _stale(target: str, deps) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def _run(cmd, verbose):
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose or res.returncode != 0:
+        sys.stderr.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
+    if res.returncode != 0:
+        raise RuntimeError(f"build step failed ({res.returncode}): {' '.join(cmd)}")
+    return res
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
+    """Compile (only what changed, unless ``force``) and link; returns the library path."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    objs, jobs = [], []
+    for src in SOURCES:
+        path = os.path.join(CSRC, src)
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        objs.append(obj)
+        if force or ptxas_verbose or _stale(obj, [path] + HEADERS):
+            jobs.append([nvcc()] + _flags(ptxas_verbose) + ["-c", path, "-o", obj])
+    with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as pool:
+        list(pool.map(lambda c: _run(c, verbose or ptxas_verbose), jobs))
+    if force or jobs or _stale(LIB, objs):
+        tmp = LIB + ".tmp"
+        _run([nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs, verbose)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, ptxas_verbose="--ptxas" in sys.argv))

@@ -1,0 +1,71 @@
+// Internal interface between the host side of the library (zero_api.cpp)
+// and its CUDA kernels (fused_step.cu, copy_cast.cu).  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zero {
+
+constexpr int kMaxRanks = 64;     // simulated ranks per context
+constexpr int kMaxSegs = 64;      // output segments per fused launch (one per rank at most)
+constexpr int kMaxCopySegs = 64;  // segments per copy / cast launch
+
+enum Dtype : int { kF16 = 0, kBF16 = 1 };
+
+// fp32 coefficients of one Adam step, derived on the host in fp64 from
+// (lr, beta1, beta2, eps, t) and rounded once each:
+//   m <- b1 m + omb1 g;  v <- b2 v + omb2 g g;
+//   theta <- theta - step_size m / (sqrt(v) rsqrt_bc2 + eps)
+// with step_size = lr / (1 - beta1^t) and rsqrt_bc2 = 1 / sqrt(1 - beta2^t),
+// which is the bias-corrected update theta - lr m_hat / (sqrt(v_hat) + eps).
+struct AdamCoef {
+  float b1, omb1, b2, omb2, step_size, rsqrt_bc2, eps, inv_w;
+};
+
+// One contiguous stretch of the flat vector whose 16-bit results go to one
+// contiguous destination: elements [lo, lo + len) of master / m / v and of
+// every rank's gradient vector; out points at the 16-bit slot of element lo.
+struct Seg {
+  int64_t lo;
+  int64_t len;
+  void* out;
+};
+
+struct FusedLaunch {
+  int W;
+  int grad_dtype, work_dtype;
+  const void* grads[kMaxRanks];   // rank w's gradient vector (flat, 16-bit)
+  float* master;
+  float* m;
+  float* v;
+  Seg segs[kMaxSegs];
+  int nseg;
+  AdamCoef coef;
+  int variant;                    // ZERO_VARIANT_*
+};
+
+// A byte range to copy, or a float range to cast.
+struct CopySeg {
+  const void* src;
+  void* dst;
+  int64_t count;                  // bytes (copy) or elements (cast)
+};
+
+// Fused reduce-scatter + Adam + recast over the given segments.
+// Returns the CUDA error of the launch; *launches counts kernels started.
+cudaError_t launch_fused_step(const FusedLaunch& a, cudaStream_t stream, int64_t* launches);
+
+// Gather: copy each segment's bytes (16-byte vectors where both ends allow).
+cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int64_t* launches);
+
+// Cast fp32 -> 16-bit (round to nearest even) for each segment.
+cudaError_t launch_cast(const CopySeg* segs, int nseg, int work_dtype, cudaStream_t stream, int64_t* launches);
+
+// Bounded device-side waits that gave up since the library was loaded.
+cudaError_t read_device_errors(unsigned int* out);
+
+// Streaming multiprocessors of the current device.
+int sm_count();
+
+}  // namespace zero
