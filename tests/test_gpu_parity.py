@@ -43,7 +43,7 @@ def test_tiny_lab_case_all_schemes():
             run.compare()
             th, m, v, p16 = run.gpu_state()
             gh.assert_f32_close(th, orc.full_master()[:8], "scheme oracle master")
-            gh.assert_ulp16(p16, orc.working_copy()[:8], "scheme oracle 16-bit")
+            gh.assert_16bit_band(p16, orc.full_master()[:8], "fp16", "scheme oracle 16-bit")
         assert zs.zero_comm_bytes_per_rank(run.zs.ctx) == orc.comm_bytes()
         assert zs.zero_comm_bytes_per_rank(run.zs.ctx) == wl.steps * z.comm_bytes_closed_form(scheme, 8, 4)
         finals.append([x.copy() for x in run.gpu_state()])
