@@ -56,6 +56,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="zero3_24x50m_w8",
                    choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1"])
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None)
+    p.add_argument("--units", type=int, default=None,
+                   help="ZeRO-3 only: keep the first N units (a smaller copy of the workload with the same "
+                        "per-unit launches, for profiling)")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -65,9 +68,12 @@ def parse_args(argv=None):
 
 # ---- workload arithmetic ----------------------------------------------------------
 
-def workload(name):
+def workload(name, units=None):
     import workloads as wk
-    return wk.WORKLOADS[name]
+    wl = wk.WORKLOADS[name]
+    if units is not None and wl.unit_sizes is not None and units < len(wl.unit_sizes):
+        wl = wk.scaled(wl, unit_sizes=wl.unit_sizes[:units], name=f"{wl.name}_first{units}units")
+    return wl
 
 
 def scheme_of(wl):
@@ -239,7 +245,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    wl = workload(args.workload)
+    wl = workload(args.workload, args.units)
     dtype = args.dtype or wl.dtypes[0]
     budget = max(0.2, 150.0 / max(1, args.steps + args.warmup))
     size = calibrate_sample(wl, dtype, budget)
@@ -298,7 +304,7 @@ def run_ours(args):
     import zero_sharded_mixed_step_gb300 as zs
     import workloads as wk
 
-    wl = workload(args.workload)
+    wl = workload(args.workload, args.units)
     dtype = args.dtype or wl.dtypes[0]
     scheme = scheme_of(wl)
     n_pad, per_launch, units = layout_sizes(wl)
