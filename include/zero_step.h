@@ -293,6 +293,42 @@ int zero_set_variant(zero_ctx* ctx, int variant);
  */
 int zero_mark_rank(zero_ctx* ctx, int rank, int available);
 
+/*
+ * ZeRO-3 step that allocates nothing.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory:
+ * code running where cudaMalloc is not allowed or not wanted (a host
+ * callback, a memory pool that is already fully reserved, a process whose
+ * device allocator belongs to another framework), which therefore cannot
+ * hand zero_step the two unit buffers ZeRO-3 gathers into.
+ *
+ * It runs the same step as zero_step does for a ZeRO-3 context - forward
+ * gathers in unit order, backward gathers in reverse order each followed by
+ * the unit's reduce-scatter + Adam + recast - all on `stream`, and gathers
+ * into a fixed 16 MiB array of device memory that belongs to the library
+ * instead of caller buffers.  Layout and arguments are those of zero_init
+ * and zero_step for ZeRO-3: master, m, v (n_pad floats, 32-byte aligned),
+ * shard16 (W shard stores of sum_u S_u values), grads (W vectors of n_pad
+ * values, 16-byte aligned); hook/user as in zero_set_unit_hook (may be
+ * NULL), called with the library's buffer.  There is no context: the caller
+ * keeps the step counter t, and the shard stores must already hold the
+ * 16-bit cast of the master (as zero_refresh_working_copy leaves them).
+ *
+ * Limits and sharing.  Each unit, padded, may hold at most 8,388,608 16-bit
+ * values (S_u * W); larger units return ZERO_E_ARG with a message, before
+ * any GPU work.  The array is held by every GPU on which the library is
+ * loaded until the process exits.  All calls share it and it keeps the last
+ * call's contents (each gather overwrites what it reads, so nothing needs
+ * clearing); calls whose work overlaps on the GPU race on it, so issue
+ * them on one stream or otherwise serialise them.  The first call on a
+ * device looks up the array's device address there (cudaGetSymbolAddress
+ * with that device current); make that first call before any stream
+ * capture.  Nothing here calls cudaMalloc, cudaFree or any other allocator.
+ */
+int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_sizes, int grad_dtype, int work_dtype,
+                        float* master, float* m, float* v, void* const* shard16, const void* const* grads,
+                        double lr, double beta1, double beta2, double eps, int64_t t,
+                        zero_unit_hook hook, void* user, void* stream);
+
 /* Message for the calling thread's last error ("" if none). */
 const char* zero_last_error(void);
 

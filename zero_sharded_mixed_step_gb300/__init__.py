@@ -62,6 +62,7 @@ SIGNATURES = {
     "zero_read_timing": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _LP]),
     "zero_set_variant": (_I, [_P, _I]),
     "zero_mark_rank": (_I, [_P, _I, _I]),
+    "zero_step_z3_static": (_I, [_I, _L, _LP, _I, _I, _P, _P, _P, _PP, _PP, _D, _D, _D, _D, _L, HOOK, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 
@@ -236,6 +237,17 @@ def zero_set_variant(ctx, variant: int) -> None:
 
 def zero_mark_rank(ctx, rank: int, available: bool) -> None:
     _check("zero_mark_rank", lib().zero_mark_rank(ctx, rank, 1 if available else 0))
+
+
+def zero_step_z3_static(W, unit_sizes, grad_dtype, work_dtype, master, m, v, shard16, grads,
+                        lr, beta1, beta2, eps, t, hook=None, stream=None) -> None:
+    """The ZeRO-3 step for callers that cannot allocate device memory: its
+    gather buffer is the library's own fixed array (units up to 8,388,608
+    padded 16-bit values); no context."""
+    cb = HOOK(hook) if hook is not None else HOOK()
+    _check("zero_step_z3_static", lib().zero_step_z3_static(
+        W, len(unit_sizes), _i64_array(unit_sizes), grad_dtype, work_dtype, _ptr(master), _ptr(m), _ptr(v),
+        _ptr_array(shard16), _ptr_array(grads), lr, beta1, beta2, eps, t, cb, None, _stream(stream)))
 
 
 # ---- convenience owner ----------------------------------------------------------

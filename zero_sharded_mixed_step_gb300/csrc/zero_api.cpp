@@ -95,6 +95,8 @@ int64_t ring_bytes(int W, int64_t S) { return int64_t(W - 1) * S * 2; }
 
 }  // namespace
 
+int zero::record_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 struct zero_ctx {
   int scheme = 0, W = 0, gdt = 0, wdt = 0;
   Layout L;

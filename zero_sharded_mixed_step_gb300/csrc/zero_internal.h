@@ -68,4 +68,7 @@ cudaError_t read_device_errors(unsigned int* out);
 // Streaming multiprocessors of the current device.
 int sm_count();
 
+// Set the calling thread's zero_last_error() message; returns code.
+int record_error(int code, const char* msg);
+
 }  // namespace zero
