@@ -197,10 +197,15 @@ int zero_refresh_working_copy(zero_ctx* ctx);
  *                     step counter + 1 (ZERO_E_STATE otherwise).
  * DP/Z1/Z2: one fused pass over the flat vector: mean of the W gradients,
  * Adam, recast into p16.  Traffic counted: 2 (W-1) S 2 bytes.
- * Z3: for u = 0..U-1 gather u (stream_gather), call the hook, release; then
- * for u = U-1..0 gather u, call the hook, update unit u (stream_update),
- * release.  The gather of the next unit overlaps the current unit's update;
- * at most two unit buffers are live.  Traffic: 3 (W-1) S_u 2 bytes per unit.
+ * Z3: for u = 0..U-1 gather u, call the hook, release; then for
+ * u = U-1..0 gather u, call the hook, update unit u (stream_update),
+ * release.  With a hook registered the gathers run on stream_gather, so the
+ * next unit's gather overlaps the work on the current one (prefetch); with
+ * none, everything runs in order on stream_update (there is no compute to
+ * hide a gather behind) and each backward gather is done by the unit's
+ * update pass, which copies the unit's 16-bit values into the unit buffer
+ * before overwriting them.  At most two unit buffers are live.  Traffic:
+ * 3 (W-1) S_u 2 bytes per unit.
  * The step is ordered after earlier work on stream_update and all its work
  * is finished when work enqueued later on stream_update starts.
  */

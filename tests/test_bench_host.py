@@ -1,0 +1,78 @@
+"""bench.py's host logic without a GPU: the replicas path's max over ranks
+and whole-job value on world_size-2 gloo ranks, the reference arm's rank
+handling, and the workload arithmetic."""
+
+import io
+import json
+import os
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = bench.max_over_ranks(10.0 + rank)            # the slowest replica sets the time
+    out[rank] = (ms, bench.whole_job_value(world, 1000, 5, ms))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_replicas_take_the_slowest_rank_over_gloo():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = 29500 + os.getpid() % 2000
+        procs = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        assert out[0] == out[1]
+        ms, value = out[0]
+        assert ms == 11.0
+        assert value == pytest.approx(2 * 1000 * 5 / 0.011)
+
+
+def test_single_process_max_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.whole_job_value(1, 10, 2, 1000.0) == 20.0
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    assert buf.getvalue() == ""
+
+
+def test_workload_bytes():
+    wl = bench.workload("zero3_24x50m_w8")
+    fused, gathers = bench.algorithmic_bytes(wl)
+    assert fused == 42 * 24 * 50_331_648 and gathers == 8 * 24 * 50_331_648
+    small = bench.workload("zero3_24x50m_w8", units=3)
+    assert small.n == 3 * 50_331_648 and bench.layout_sizes(small)[1] == [50_331_648] * 3
+    xl = bench.workload("gpt2_1p5b_w16_zero1")
+    assert bench.algorithmic_bytes(xl) == (58 * 1_557_611_200, 0)
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch):
+    monkeypatch.delenv("RANK", raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1", "--reference-seconds", "1",
+                           "--workload", "gpt2_small_124m_w8_zero2"]) == 0
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "params/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["metric"] == bench.METRIC

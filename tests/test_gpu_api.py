@@ -141,7 +141,34 @@ def test_rank_fault_injection_launches_nothing():
     zs.zero_mark_rank(s.ctx, 3, True)
     s.step(grads[0], wl.lr, wl.beta1, wl.beta2, wl.eps, 1)
     s.sync()
-    assert s.stat(zs.ZERO_STAT_LAUNCHES) == n0 + 3 * 2
+    # no hook: a forward gather per unit, and one pass per unit that gathers and updates
+    assert s.stat(zs.ZERO_STAT_LAUNCHES) == n0 + 2 * 2
+    s.close()
+
+
+def test_zero3_backward_gather_fused_into_update():
+    """Without a unit hook the backward gather of each unit is done by the
+    unit's update pass: after the step the two unit buffers hold the last two
+    units gathered (units 1 and 0, in backward order) as they were before the
+    update, bit for bit, and the traffic counts three collectives per unit."""
+    units = [100_003, 65_536, 70_001]
+    wl = wk.scaled(wk.LAYER_UNITS, unit_sizes=units, steps=2, name="fused_gather")
+    s = zs.ZeroStep(zs.ZERO_SCHEME_Z3, wl.W, units, "bf16", theta0=wk.draw_theta0(wl, "cuda"))
+    grads = _grads(wl, "bf16", 2, s)
+    for t in (1, 2):
+        torch.cuda.synchronize()
+        before = s.working_copy().clone()
+        s.step(grads[t - 1], wl.lr, wl.beta1, wl.beta2, wl.eps, t)
+        torch.cuda.synchronize()
+        U = len(units)
+        for u, seq in ((1, 2 * U - 2), (0, 2 * U - 1)):
+            buf = s.unit_bufs[seq & 1]
+            o, sh = s.off[u], s.shard[u]
+            assert torch.equal(buf[: sh * wl.W].view(torch.int16), before[o:o + sh * wl.W].view(torch.int16)), (t, u)
+        assert not torch.equal(before, s.working_copy())
+    L = z.Layout(wl.W, units)
+    assert zs.zero_comm_bytes_per_rank(s.ctx) == 2 * 3 * sum(z.ring_bytes_per_rank(wl.W, x) for x in L.S)
+    assert s.stat(zs.ZERO_STAT_LAUNCHES) == len(units) + 2 * 2 * len(units)   # a cast per unit + 2 per unit per step
     s.close()
 
 

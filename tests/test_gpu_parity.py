@@ -122,17 +122,29 @@ def test_schemes_bit_identical_on_gpu():
 
 
 def test_zero3_overlap_equals_serial():
-    """The ZeRO-3 step with a separate gather stream (overlapped) and on one
-    stream (serial) give bit-identical results."""
+    """The ZeRO-3 step with a unit hook (gathers on their own stream, each
+    overlapping the work on the unit before) and without one (everything in
+    order on one stream, each backward gather done by the unit's update
+    pass) give bit-identical results."""
     units = [65_536 * 3 + 5] * 6
     wl = wk.scaled(wk.LAYER_UNITS, unit_sizes=units, steps=3, name="overlap")
     out = []
-    for gather_stream in (True, False):
-        run = gh.Run(wl, zs.ZERO_SCHEME_Z3, "bf16", units=units, sample=np.arange(wl.n),
-                     gather_stream=gather_stream)
+    for with_hook in (True, False):
+        run = gh.Run(wl, zs.ZERO_SCHEME_Z3, "bf16", units=units, sample=np.arange(wl.n), gather_stream=True)
+        sums = []
+        if with_hook:
+            def hook(_user, phase, unit, buf, stream):
+                s = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
+                with torch.cuda.stream(s):
+                    b = next(x for x in run.zs.unit_bufs if x.data_ptr() == buf)
+                    sums.append(b.float().abs().sum())       # some work that reads the gathered unit
+            run.zs.set_unit_hook(hook)
         for _ in range(wl.steps):
             run.step()
         run.compare()
+        if with_hook:
+            torch.cuda.synchronize()
+            assert len(sums) == 2 * len(units) * wl.steps and all(bool(torch.isfinite(x)) for x in sums)
         out.append([x.copy() for x in run.gpu_state()])
         run.close()
     for a, b in zip(*out):

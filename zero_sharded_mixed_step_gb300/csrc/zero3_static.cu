@@ -132,7 +132,7 @@ extern "C" int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_s
     if (hook) hook(user, phase, u, buf, stream);
     if (phase == 1) {
       a.nseg = W;
-      for (int r = 0; r < W; ++r) a.segs[r] = {off + r * S, S, static_cast<char*>(shard16[r]) + off16 * 2};
+      for (int r = 0; r < W; ++r) a.segs[r] = {off + r * S, S, static_cast<char*>(shard16[r]) + off16 * 2, nullptr};
       e = zero::launch_fused_step(a, s, &launches);
       if (e != cudaSuccess) return set_error(ZERO_E_CUDA, cudaGetErrorString(e));
     }

@@ -211,9 +211,11 @@ zero::AdamCoef make_coef(double lr, double b1, double b2, double eps, int64_t t,
   return c;
 }
 
-// The fused pass over unit u (or, for DP/Z1/Z2, the whole vector).
+// The fused pass over unit u (or, for DP/Z1/Z2, the whole vector).  With
+// gather_dst set (ZeRO-3 only), the same pass first copies unit u's current
+// 16-bit shards into gather_dst, in flat order: the unit's gather.
 int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const zero::AdamCoef& coef,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, void* gather_dst = nullptr) {
   zero::FusedLaunch a;
   std::memset(&a, 0, sizeof a);
   a.W = c->W;
@@ -229,14 +231,15 @@ int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const zero::
   if (c->scheme != ZERO_SCHEME_Z3) {
     // one stretch: the recast goes straight to its place in the full vector
     a.nseg = c->L.n_pad > 0 ? 1 : 0;
-    a.segs[0] = {0, c->L.n_pad, c->p16};
+    a.segs[0] = {0, c->L.n_pad, c->p16, nullptr};
   } else {
     // rank r's slice of the unit goes to r's own 16-bit shard store
     a.nseg = 0;
     for (int r = 0; r < c->W; ++r) {
       if (S == 0) break;
       char* dst = static_cast<char*>(c->shard16[r]) + c->L.off16[u] * 2;
-      a.segs[a.nseg++] = {off + r * S, S, dst};
+      void* pre = gather_dst ? static_cast<char*>(gather_dst) + r * S * 2 : nullptr;
+      a.segs[a.nseg++] = {off + r * S, S, dst, pre};
     }
   }
   Bracket br{c, ZERO_KERNEL_FUSED, stream};
@@ -282,14 +285,20 @@ void live_add(zero_ctx* c, int64_t elems) {
 // ZeRO-3 step: forward gathers in unit order, backward gathers in reverse
 // order each followed by the unit's update, two gather buffers in turn.  The
 // gather of the next unit (stream G) waits only for the buffer it reuses to
-// be released by stream A, so it overlaps the current unit's work.  A unit
-// counts as live from its gather until its buffer is taken by a later gather
-// (or the step ends): at most two units are live.
+// be released by stream A, so it overlaps the current unit's work (the
+// prefetch of "ZeRO and FSDP").  That overlap is there to hide a gather
+// behind the caller's compute on the unit before it, so it is used when a
+// unit hook is registered; with no hook the only work on stream A is the
+// memory-bound update, and running the gathers beside it on GB300 measured
+// slower than running everything in order on stream A.  A unit counts as live
+// from its gather until its buffer is taken by a later gather (or the step
+// ends): at most two units are live.
 int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& coef) {
   int rc = ensure_cuda(c);
   if (rc) return rc;
-  cudaStream_t su = c->su, sg = c->sg;
-  const bool two_streams = sg != su;
+  cudaStream_t su = c->su;
+  const bool two_streams = c->sg != su && c->hook != nullptr;
+  cudaStream_t sg = two_streams ? c->sg : su;
   if (two_streams) {
     ZERO_CUDA(cudaEventRecord(c->ev_begin, su));
     ZERO_CUDA(cudaStreamWaitEvent(sg, c->ev_begin, 0));
@@ -303,11 +312,21 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
     void* buf = c->ubuf[b];
     if (used[b] && two_streams) ZERO_CUDA(cudaStreamWaitEvent(sg, c->ev_free[b], 0));
     c->live_elems -= held[b];
-    int r = launch_gather(c, u, buf, sg);
-    if (r) return r;
     held[b] = c->L.shard[u] * c->W;
     live_add(c, held[b]);
     count_gather(c, u);
+    int r = ZERO_OK;
+    if (phase == 1 && c->hook == nullptr) {
+      // nothing runs between this unit's gather and its update, so one pass
+      // does both: it copies the pre-update 16-bit values out, then updates
+      r = launch_update(c, u, grads, coef, su, buf);
+      if (r) return r;
+      count_scatter(c, u);
+      used[b] = true;
+      return ZERO_OK;
+    }
+    r = launch_gather(c, u, buf, sg);
+    if (r) return r;
     if (two_streams) {
       ZERO_CUDA(cudaEventRecord(c->ev_gathered[b], sg));
       ZERO_CUDA(cudaStreamWaitEvent(su, c->ev_gathered[b], 0));

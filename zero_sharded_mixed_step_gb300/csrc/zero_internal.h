@@ -26,10 +26,13 @@ struct AdamCoef {
 // One contiguous stretch of the flat vector whose 16-bit results go to one
 // contiguous destination: elements [lo, lo + len) of master / m / v and of
 // every rank's gradient vector; out points at the 16-bit slot of element lo.
+// When pre_out is set, the 16-bit value held at out before the update is
+// first copied to pre_out (the ZeRO-3 backward gather of the same unit).
 struct Seg {
   int64_t lo;
   int64_t len;
   void* out;
+  void* pre_out;
 };
 
 struct FusedLaunch {
