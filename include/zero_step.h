@@ -81,8 +81,9 @@ extern "C" {
 #define ZERO_PEAK       1
 
 /* ---- kernel variants for the fused reduce + Adam + cast pass ------------ */
-#define ZERO_VARIANT_AUTO   0  /* the fastest measured variant                    */
+#define ZERO_VARIANT_AUTO   0  /* the fastest measured variant for the launch     */
 #define ZERO_VARIANT_VECTOR 1  /* 256-bit vector loads into registers             */
+#define ZERO_VARIANT_BULK   2  /* bulk async copies into a shared-memory ring     */
 
 /* ---- statistics (zero_stat) --------------------------------------------- */
 #define ZERO_STAT_COMM_BYTES      0  /* bytes a rank would send, cumulative       */
@@ -92,7 +93,10 @@ extern "C" {
 #define ZERO_STAT_LIVE_ELEMS      4  /* gathered 16-bit elements live right now   */
 #define ZERO_STAT_PEAK_LIVE_ELEMS 5  /* most gathered elements ever live at once  */
 #define ZERO_STAT_T               6  /* the last step counter used                */
-#define ZERO_STAT_DEVICE_ERRORS   7  /* bounded waits that gave up (see variants) */
+#define ZERO_STAT_DEVICE_ERRORS   7  /* bounded device waits of this context's
+                                        launches that gave up                       */
+#define ZERO_STAT_LAST_VARIANT    8  /* kernel of the last fused launch: ZERO_VARIANT_VECTOR
+                                        or ZERO_VARIANT_BULK (0 before any)          */
 
 typedef struct zero_ctx zero_ctx;
 
@@ -287,8 +291,26 @@ int zero_enable_timing(zero_ctx* ctx, int on);
  */
 int zero_read_timing(zero_ctx* ctx, int kernel, double* total_ms, int64_t* launches);
 
-/* Select the fused-pass variant (ZERO_VARIANT_*). */
+/*
+ * Select the fused-pass variant (ZERO_VARIANT_*).  AUTO uses the bulk-staged
+ * kernel where it measured faster (W of 8 or 16, at least one 2048-element
+ * tile) and the vector kernel elsewhere.  BULK asks for the bulk-staged
+ * kernel; it still runs the vector kernel where the bulk one cannot (W not
+ * in {1, 2, 4, 8, 16}, or 16-bit slots not 16-byte aligned).  Both give
+ * bit-identical results.
+ */
 int zero_set_variant(zero_ctx* ctx, int variant);
+
+/*
+ * Testing the bounded device waits.  The next fused launch of this context,
+ * if it runs the bulk-staged kernel, never loads tile `tile` of its first
+ * CTA: that CTA's wait for it runs out after about a second, the CTA counts
+ * a device error, waits (bounded) for the copies it did issue and returns.
+ * zero_sync then returns ZERO_E_STATE and the context stays usable; the
+ * values that launch should have written are not valid.  Nothing faults or
+ * hangs.  tile < 0 cancels a pending injection.
+ */
+int zero_inject_stall(zero_ctx* ctx, int64_t tile);
 
 /*
  * Host-side fault injection: mark simulated rank `rank` unavailable

@@ -99,7 +99,7 @@ class Run:
     or a sample of them)."""
 
     def __init__(self, wl: wk.Workload, scheme: int, dtype: str, units=None, sample=None,
-                 gather_stream: bool = True, work_dtype: str | None = None):
+                 gather_stream: bool = True, work_dtype: str | None = None, variant: int = 0):
         self.wl, self.scheme, self.dtype = wl, scheme, dtype
         self.work_dtype = work_dtype or dtype
         self.units = list(units) if units is not None else (wl.units() if scheme == zs.ZERO_SCHEME_Z3 else [wl.n])
@@ -108,6 +108,7 @@ class Run:
         self.gs = torch.cuda.Stream() if gather_stream and scheme == zs.ZERO_SCHEME_Z3 else None
         self.zs = zs.ZeroStep(scheme, wl.W, self.units, dtype, self.work_dtype, theta0=theta0, device=dev,
                               gather_stream=self.gs, with_grad_buffers=True)
+        self.zs.set_variant(variant)
         self.src = wk.GradSource(wl, dtype, dev)
         self.real_idx = self.zs.real_index()
         self.full = sample is None

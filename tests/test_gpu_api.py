@@ -188,3 +188,28 @@ def test_tiny_and_empty_vectors():
             run.compare()
         assert run.padding_is_zero()
         run.close()
+
+
+def test_bounded_device_wait_reports_and_recovers():
+    """A bulk-staged launch whose tile never loads (injected on purpose) gives
+    up after its bounded wait instead of hanging: zero_sync reports
+    ZERO_E_STATE, the device error count rises, and the context keeps
+    working for the next steps."""
+    n, W = 8 * 2048 * 200, 8
+    wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=3, name="stall")
+    s = zs.ZeroStep(zs.ZERO_SCHEME_Z2, W, [n], "bf16", theta0=wk.draw_theta0(wl, "cuda"))
+    s.set_variant(zs.ZERO_VARIANT_BULK)
+    grads = _grads(wl, "bf16", 3, s)
+    s.step(grads[0], wl.lr, wl.beta1, wl.beta2, wl.eps, 1)
+    s.sync(timeout_ms=60_000)
+    assert s.stat(zs.ZERO_STAT_DEVICE_ERRORS) == 0 and s.stat(zs.ZERO_STAT_LAST_VARIANT) == zs.ZERO_VARIANT_BULK
+    zs.zero_inject_stall(s.ctx, 1)
+    s.step(grads[1], wl.lr, wl.beta1, wl.beta2, wl.eps, 2)
+    with pytest.raises(zs.ZeroError) as e:
+        s.sync(timeout_ms=60_000)
+    assert e.value.code == zs.ZERO_E_STATE and "bounded device waits" in str(e.value)
+    assert s.stat(zs.ZERO_STAT_DEVICE_ERRORS) == 1
+    s.step(grads[2], wl.lr, wl.beta1, wl.beta2, wl.eps, 3)     # still usable, and no new error
+    s.sync(timeout_ms=60_000)
+    assert s.stat(zs.ZERO_STAT_DEVICE_ERRORS) == 1
+    s.close()

@@ -83,23 +83,54 @@ RAGGED = [
 ]
 
 
+VARIANTS = {"auto": zs.ZERO_VARIANT_AUTO, "vector": zs.ZERO_VARIANT_VECTOR, "bulk": zs.ZERO_VARIANT_BULK}
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("case", RAGGED, ids=lambda c: f"n{c[0]}_W{c[1]}_s{c[2]}_{c[3]}_{c[4]}")
-def test_ragged_full_compare(case):
+def test_ragged_full_compare(case, variant):
     """Sizes that leave ragged tails, W that is not a power of two (the mean
     divides), W = 64 (any-W path), mixed gradient / working-copy formats,
     ZeRO-3 units with padding and an empty unit: every element for 4 steps,
-    padding exactly zero."""
+    padding exactly zero, under each fused-kernel variant."""
     n, W, scheme, gdt, wdt, units = case
     if units is not None:
         n = sum(units)
     wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=4, unit_sizes=units, name=f"ragged_{n}_{W}",
                    outlier_frac=1e-3)
-    run = gh.Run(wl, scheme, gdt, units=units, work_dtype=wdt)
+    run = gh.Run(wl, scheme, gdt, units=units, work_dtype=wdt, variant=VARIANTS[variant])
     for _ in range(wl.steps):
         run.step()
         run.compare()
     assert run.padding_is_zero()
     run.close()
+
+
+@pytest.mark.parametrize("case", [(124_439_808, 8, zs.ZERO_SCHEME_Z2, "bf16", None),
+                                  (50_331_651, 16, zs.ZERO_SCHEME_Z1, "fp16", None),
+                                  (None, 8, zs.ZERO_SCHEME_Z3, "bf16", [50_331_648, 6_291_459, 4096]),
+                                  (3_000_005, 4, zs.ZERO_SCHEME_DP, "bf16", None)],
+                         ids=["gpt2small_w8", "w16_ragged", "zero3_w8", "w4"])
+def test_bulk_and_vector_kernels_bit_identical(case):
+    """The bulk-staged and the register kernel leave the same bits in every
+    element, full-size GPT-2-small included, and report which one ran."""
+    n, W, scheme, dtype, units = case
+    if units is not None:
+        n = sum(units)
+    wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=2, unit_sizes=units, name="variants")
+    states = []
+    for variant in (zs.ZERO_VARIANT_VECTOR, zs.ZERO_VARIANT_BULK):
+        run = gh.Run(wl, scheme, dtype, units=units, sample=np.arange(min(n, 4096)), variant=variant)
+        for _ in range(wl.steps):
+            run.step()
+        torch.cuda.synchronize()
+        assert run.zs.stat(zs.ZERO_STAT_LAST_VARIANT) == variant
+        states.append([x.clone() for x in (run.zs.master, run.zs.m, run.zs.v, run.zs.working_copy())])
+        run.compare()
+        run.close()
+    for a, b in zip(*states):
+        assert torch.equal(a.view(torch.int16) if a.element_size() == 2 else a.view(torch.int32),
+                           b.view(torch.int16) if b.element_size() == 2 else b.view(torch.int32))
 
 
 def test_schemes_bit_identical_on_gpu():

@@ -26,9 +26,9 @@ ZERO_OK, ZERO_E_ARG, ZERO_E_ALIGN, ZERO_E_CUDA, ZERO_E_RANK, ZERO_E_TIMEOUT, ZER
 ZERO_SCHEME_DP, ZERO_SCHEME_Z1, ZERO_SCHEME_Z2, ZERO_SCHEME_Z3 = 0, 1, 2, 3
 ZERO_FP16, ZERO_BF16 = 0, 1
 ZERO_RESIDENT, ZERO_PEAK = 0, 1
-ZERO_VARIANT_AUTO, ZERO_VARIANT_VECTOR = 0, 1
+ZERO_VARIANT_AUTO, ZERO_VARIANT_VECTOR, ZERO_VARIANT_BULK = 0, 1, 2
 (ZERO_STAT_COMM_BYTES, ZERO_STAT_LAUNCHES, ZERO_STAT_GATHERS, ZERO_STAT_SCATTERS, ZERO_STAT_LIVE_ELEMS,
- ZERO_STAT_PEAK_LIVE_ELEMS, ZERO_STAT_T, ZERO_STAT_DEVICE_ERRORS) = range(8)
+ ZERO_STAT_PEAK_LIVE_ELEMS, ZERO_STAT_T, ZERO_STAT_DEVICE_ERRORS, ZERO_STAT_LAST_VARIANT) = range(9)
 ZERO_MAX_RANKS = 64
 ZERO_KERNEL_FUSED, ZERO_KERNEL_GATHER, ZERO_KERNEL_CAST = 0, 1, 2
 
@@ -61,6 +61,7 @@ SIGNATURES = {
     "zero_enable_timing": (_I, [_P, _I]),
     "zero_read_timing": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _LP]),
     "zero_set_variant": (_I, [_P, _I]),
+    "zero_inject_stall": (_I, [_P, _L]),
     "zero_mark_rank": (_I, [_P, _I, _I]),
     "zero_step_z3_static": (_I, [_I, _L, _LP, _I, _I, _P, _P, _P, _PP, _PP, _D, _D, _D, _D, _L, HOOK, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
@@ -235,6 +236,10 @@ def zero_set_variant(ctx, variant: int) -> None:
     _check("zero_set_variant", lib().zero_set_variant(ctx, variant))
 
 
+def zero_inject_stall(ctx, tile: int) -> None:
+    _check("zero_inject_stall", lib().zero_inject_stall(ctx, tile))
+
+
 def zero_mark_rank(ctx, rank: int, available: bool) -> None:
     _check("zero_mark_rank", lib().zero_mark_rank(ctx, rank, 1 if available else 0))
 
@@ -333,6 +338,9 @@ class ZeroStep:
 
     def set_unit_hook(self, fn):
         self._hook = zero_set_unit_hook(self.ctx, fn)
+
+    def set_variant(self, variant):
+        zero_set_variant(self.ctx, variant)
 
     def stat(self, which):
         return zero_stat(self.ctx, which)

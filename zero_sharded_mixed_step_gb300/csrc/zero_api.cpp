@@ -8,6 +8,7 @@
 
 #include <chrono>
 #include <cmath>
+#include <mutex>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -93,6 +94,27 @@ int64_t resident_bytes(int scheme, int64_t n, int64_t S) {
 // ZeRO", appendix B).
 int64_t ring_bytes(int W, int64_t S) { return int64_t(W - 1) * S * 2; }
 
+// Counter slots for bounded device waits: slot 0 belongs to no context, the
+// others are handed to contexts while they live; when all are taken, new
+// contexts share the last one.
+std::mutex g_slot_mu;
+bool g_slot_used[zero::kErrSlots] = {true};
+
+int take_slot() {
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  for (int i = 1; i < zero::kErrSlots; ++i)
+    if (!g_slot_used[i]) {
+      g_slot_used[i] = true;
+      return i;
+    }
+  return zero::kErrSlots - 1;
+}
+
+void give_slot(int i) {
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  if (i > 0 && i < zero::kErrSlots - 1) g_slot_used[i] = false;
+}
+
 }  // namespace
 
 int zero::record_error(int code, const char* msg) { return fail(code, "%s", msg); }
@@ -118,6 +140,12 @@ struct zero_ctx {
   zero_unit_hook hook = nullptr;
   void* hook_user = nullptr;
   bool timing = false;
+  bool stall_pending = false;
+  int64_t stall_tile = -1;
+  int err_slot = 0;            // this context's device error counter slot
+  bool err_slot_ready = false; // cleared on the device (at the first fused launch)
+  int64_t dev_err_seen = 0;    // count at the last zero_sync
+  int last_variant = 0;
   std::vector<cudaEvent_t> event_pool;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[3];
 };
@@ -227,6 +255,17 @@ int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const zero::
   a.v = c->v;
   a.coef = coef;
   a.variant = c->variant;
+  if (c->stall_pending) {
+    a.inject_stall = 1;
+    a.stall_tile = c->stall_tile;
+    c->stall_pending = false;
+  }
+  a.err_slot = c->err_slot;
+  if (!c->err_slot_ready) {
+    cudaError_t e0 = zero::reset_device_errors(c->err_slot, stream);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "clearing the device error counter");
+    c->err_slot_ready = true;
+  }
   const int64_t S = c->L.shard[u], off = c->L.off[u];
   if (c->scheme != ZERO_SCHEME_Z3) {
     // one stretch: the recast goes straight to its place in the full vector
@@ -247,6 +286,7 @@ int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const zero::
   if (rc) return rc;
   cudaError_t e = zero::launch_fused_step(a, stream, &c->launches);
   if (e != cudaSuccess) return cuda_fail(e, "fused reduce-scatter/Adam/recast launch");
+  c->last_variant = zero::last_fused_variant();
   touch(c, stream);
   return br.close();
 }
@@ -474,6 +514,7 @@ int zero_init(zero_ctx** out, int scheme, int W, int64_t n, int64_t n_units, con
   c->sg = stream_gather ? static_cast<cudaStream_t>(stream_gather) : c->su;
   c->live.assign(static_cast<size_t>(n_units), 0);
   c->rank_up.assign(static_cast<size_t>(W), 1);
+  c->err_slot = take_slot();
   *out = c;
   return ZERO_OK;
 }
@@ -488,6 +529,7 @@ int zero_destroy(zero_ctx* c) {
       cudaEventDestroy(pr.second);
     }
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+  give_slot(c->err_slot);
   if (c->cuda_ready) {
     cudaEventDestroy(c->ev_begin);
     for (int b = 0; b < 2; ++b) {
@@ -659,11 +701,13 @@ int64_t zero_stat(const zero_ctx* c, int which) {
     case ZERO_STAT_PEAK_LIVE_ELEMS: return c->peak_live;
     case ZERO_STAT_T: return c->t;
     case ZERO_STAT_DEVICE_ERRORS: {
+      if (!c->err_slot_ready) return 0;
       unsigned int n = 0;
-      cudaError_t e = zero::read_device_errors(&n);
+      cudaError_t e = zero::read_device_errors(c->err_slot, &n);
       if (e != cudaSuccess) return cuda_fail(e, "reading the device error counter");
       return static_cast<int64_t>(n);
     }
+    case ZERO_STAT_LAST_VARIANT: return c->last_variant;
     default: return fail(ZERO_E_ARG, "unknown statistic %d", which);
   }
 }
@@ -703,10 +747,16 @@ int zero_sync(zero_ctx* c, int timeout_ms) {
   }
   for (cudaEvent_t e : evs) cudaEventDestroy(e);
   if (rc) return rc;
+  if (!c->err_slot_ready) return ZERO_OK;   // nothing of ours has run a bounded wait
   unsigned int nerr = 0;
-  cudaError_t e = zero::read_device_errors(&nerr);
+  cudaError_t e = zero::read_device_errors(c->err_slot, &nerr);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error counter");
-  if (nerr) return fail(ZERO_E_STATE, "%u bounded device waits gave up", nerr);
+  if (static_cast<int64_t>(nerr) > c->dev_err_seen) {
+    const int64_t fresh = static_cast<int64_t>(nerr) - c->dev_err_seen;
+    c->dev_err_seen = nerr;
+    return fail(ZERO_E_STATE, "%lld bounded device waits gave up; the work they belonged to is incomplete",
+                (long long)fresh);
+  }
   return ZERO_OK;
 }
 
@@ -741,9 +791,16 @@ int zero_read_timing(zero_ctx* c, int kernel, double* total_ms, int64_t* launche
 
 int zero_set_variant(zero_ctx* c, int variant) {
   if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
-  if (variant != ZERO_VARIANT_AUTO && variant != ZERO_VARIANT_VECTOR)
+  if (variant != ZERO_VARIANT_AUTO && variant != ZERO_VARIANT_VECTOR && variant != ZERO_VARIANT_BULK)
     return fail(ZERO_E_ARG, "unknown variant %d", variant);
   c->variant = variant;
+  return ZERO_OK;
+}
+
+int zero_inject_stall(zero_ctx* c, int64_t tile) {
+  if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
+  c->stall_pending = tile >= 0;
+  c->stall_tile = tile;
   return ZERO_OK;
 }
 

@@ -46,7 +46,19 @@ struct FusedLaunch {
   int nseg;
   AdamCoef coef;
   int variant;                    // ZERO_VARIANT_*
+  // Testing the bounded waits: with inject_stall set, the bulk-staged kernel's
+  // first CTA never loads its tile number stall_tile, so its wait runs out.
+  int inject_stall;
+  int64_t stall_tile;
+  // Counter slot that bounded waits which give up increment (0: no context).
+  int err_slot;
 };
+
+// Device-side counters of bounded waits that gave up, one slot per context.
+constexpr int kErrSlots = 1024;
+
+// Which fused kernel a launch used (ZERO_VARIANT_VECTOR or ZERO_VARIANT_BULK).
+int last_fused_variant();
 
 // A byte range to copy, or a float range to cast.
 struct CopySeg {
@@ -65,8 +77,11 @@ cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int6
 // Cast fp32 -> 16-bit (round to nearest even) for each segment.
 cudaError_t launch_cast(const CopySeg* segs, int nseg, int work_dtype, cudaStream_t stream, int64_t* launches);
 
-// Bounded device-side waits that gave up since the library was loaded.
-cudaError_t read_device_errors(unsigned int* out);
+// Clear a context's counter slot, in order on `stream` (asynchronous).
+cudaError_t reset_device_errors(int slot, cudaStream_t stream);
+
+// Read a counter slot (synchronous; call after the work has finished).
+cudaError_t read_device_errors(int slot, unsigned int* out);
 
 // Streaming multiprocessors of the current device.
 int sm_count();
