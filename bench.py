@@ -56,6 +56,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="zero3_24x50m_w8",
                    choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1"])
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None)
+    p.add_argument("--params", type=int, default=None,
+                   help="flat workloads only: a smaller copy with this many parameters (same W, dtype, "
+                        "distributions and kernel), for profiling")
     p.add_argument("--units", type=int, default=None,
                    help="ZeRO-3 only: keep the first N units (a smaller copy of the workload with the same "
                         "per-unit launches, for profiling)")
@@ -70,11 +73,13 @@ def parse_args(argv=None):
 
 # ---- workload arithmetic ----------------------------------------------------------
 
-def workload(name, units=None):
+def workload(name, units=None, params=None):
     import workloads as wk
     wl = wk.WORKLOADS[name]
     if units is not None and wl.unit_sizes is not None and units < len(wl.unit_sizes):
         wl = wk.scaled(wl, unit_sizes=wl.unit_sizes[:units], name=f"{wl.name}_first{units}units")
+    if params is not None and wl.unit_sizes is None and params < wl.n:
+        wl = wk.scaled(wl, n=params, name=f"{wl.name}_{params}params")
     return wl
 
 
@@ -247,7 +252,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    wl = workload(args.workload, args.units)
+    wl = workload(args.workload, args.units, args.params)
     dtype = args.dtype or wl.dtypes[0]
     budget = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
     size = calibrate_sample(wl, dtype, budget)
@@ -328,7 +333,7 @@ def run_ours(args):
     import zero_sharded_mixed_step_gb300 as zs
     import workloads as wk
 
-    wl = workload(args.workload, args.units)
+    wl = workload(args.workload, args.units, args.params)
     dtype = args.dtype or wl.dtypes[0]
     scheme = scheme_of(wl)
     n_pad, per_launch, units = layout_sizes(wl)
@@ -383,6 +388,7 @@ def run_ours(args):
         ms, launches = timed_pass(False)
     ms_instr, _ = timed_pass(True)
     fused_ms, fused_n = zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_FUSED)
+    last_variant = step.stat(zs.ZERO_STAT_LAST_VARIANT)
     gather_ms, gather_n = zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_GATHER)
     ms = max_over_ranks(ms)
     ms_per_step = ms / args.steps
@@ -399,7 +405,8 @@ def run_ours(args):
     fused_avg_ms = fused_ms / max(1, fused_n)
     achieved = per_launch_bytes / (fused_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": recorded_traffic("fused_step.cu", wl.name), "kernel": "fused_step_vector",
+                "traffic": recorded_traffic("fused_step.cu", wl.name),
+                "kernel": "fused_step_bulk" if last_variant == zs.ZERO_VARIANT_BULK else "fused_step_vector",
                 "peak_source": f"{peak_src} copy bandwidth", "launch_ms": fused_avg_ms,
                 "algorithmic_bytes_per_launch": per_launch_bytes, "bytes_per_element": per_elem,
                 "frac_of_8tbs_nominal": achieved / 8000.0,
