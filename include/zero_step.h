@@ -219,6 +219,49 @@ int zero_step(zero_ctx* ctx, int scheme, int W, int64_t n, const void* const* gr
 /* Register (fn != NULL) or clear the ZeRO-3 unit hook. */
 int zero_set_unit_hook(zero_ctx* ctx, zero_unit_hook fn, void* user);
 
+/* ---- the step fed from host memory ---------------------------------------- */
+
+/*
+ * Device bytes of the staging ring zero_step_host needs: two slots, each
+ * holding every rank's gradients for one chunk (DP/Z1/Z2: chunk_elems
+ * values, 0 meaning 16,777,216; ZeRO-3: one unit, max_u S_u * W values), in
+ * the gradient format: 2 * W * round_up((chunk + 8) * 2, 256).  The ring
+ * stays this size whatever n is: the constant-size buffers of "One Poem
+ * Suffices: ZeRO" section 4.2.2 (C_B) instead of W full gradient vectors on
+ * the device.  Negative on a bad argument.
+ */
+int64_t zero_host_staging_bytes(int scheme, int W, int64_t n_units, const int64_t* unit_sizes, int64_t chunk_elems);
+
+/*
+ * One ZeRO step whose gradients are in host memory and whose updated 16-bit
+ * working copy is written back to host memory.  The step is cut into chunks
+ * (DP/Z1/Z2: chunk_elems of the flat vector; ZeRO-3: one unit, backward
+ * order) and pipelined over three streams: the gradients of chunk k + 1
+ * cross the host link into the staging ring on stream_h2d while chunk k is
+ * updated on the context's update stream and chunk k - 1's results return
+ * on stream_d2h.  The arithmetic is that of zero_step (bit-identical).
+ *   scheme, W, n, lr, beta1, beta2, eps, t   as for zero_step.
+ *   host_grads   host array of W host pointers, rank w's n_pad gradient
+ *                values in flat order (pinned memory for full speed;
+ *                pageable memory works but its copies are synchronous).
+ *   host_out     host buffer for the updated working copy, or NULL: DP/Z1/Z2
+ *                n_pad values in flat order; ZeRO-3 each rank's shard store,
+ *                rank after rank (W * sum_u S_u values).
+ *   staging      device buffer of at least zero_host_staging_bytes(...)
+ *                bytes, 256-byte aligned; staging_bytes its size.
+ *   chunk_elems  as given to zero_host_staging_bytes (ignored for ZeRO-3).
+ *   stream_h2d, stream_d2h  cudaStream_t for the two copy directions (NULL
+ *                for either: the update stream, without overlap).
+ * ZeRO-3 runs the unit schedule of zero_step without a hook: forward gathers,
+ * then per unit (reverse order) one pass that gathers and updates.  When the
+ * call returns, the work is enqueued; work enqueued later on the update stream
+ * runs after all of it, copies included.  ZERO_E_ARG if the staging is too
+ * small or misaligned; the other errors as for zero_step.
+ */
+int zero_step_host(zero_ctx* ctx, int scheme, int W, int64_t n, const void* const* host_grads, void* host_out,
+                   void* staging, int64_t staging_bytes, int64_t chunk_elems, double lr, double beta1,
+                   double beta2, double eps, int64_t t, void* stream_h2d, void* stream_d2h);
+
 /* ---- ZeRO-3 driven by the caller ---------------------------------------- */
 
 /*

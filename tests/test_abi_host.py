@@ -200,3 +200,33 @@ def test_last_error_is_per_thread(zlib):
     th.join()
     assert seen["msg"] == "" and "scheme" in zs.zero_last_error()
     assert isinstance(ctypes.c_int64(zs.zero_comm_bytes_closed_form(0, 8, 4)).value, int)
+
+
+def test_host_staging_bytes(zlib):
+    # two slots x W ranks x round_up((chunk + 8) * 2, 256)
+    assert zs.zero_host_staging_bytes(1, 8, [10_000_000], 1 << 20) == 2 * 8 * (((1 << 20) + 8) * 2 + 255) // 256 * 256
+    assert zs.zero_host_staging_bytes(1, 4, [100], 0) == 2 * 4 * (((1 << 24) + 8) * 2 + 255) // 256 * 256
+    assert zs.zero_host_staging_bytes(2, 8, [100], 13) == 2 * 8 * 256       # chunk rounds up to 16 elements
+    units = [50_331_648] * 24
+    assert zs.zero_host_staging_bytes(3, 8, units, 0) == 2 * 8 * ((50_331_648 + 8) * 2 + 255) // 256 * 256
+    assert _err(zs.zero_host_staging_bytes, 1, 8, [10, 10], 0) == zs.ZERO_E_ARG
+    assert _err(zs.zero_host_staging_bytes, 1, 8, [10], -1) == zs.ZERO_E_ARG
+
+
+def test_step_host_checks_before_any_launch(zlib):
+    c = make_ctx(scheme=1, W=4, units=(1000,))
+    need = zs.zero_host_staging_bytes(1, 4, [1000], 256)
+    hg = [fake(50 + r) for r in range(4)]
+    hp = (1e-3, 0.9, 0.999, 1e-8)
+    st = fake(60)
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, st, need - 1, 256, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, st + 16, need, 256, *hp, 1) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, None, need, 256, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg[:3] + [None], None, st, need, 256, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step_host, c, 2, 4, 1000, hg, None, st, need, 256, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, st, need, 256, *hp, 2) == zs.ZERO_E_STATE
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, st, need, -5, *hp, 1) == zs.ZERO_E_ARG
+    zs.zero_mark_rank(c, 1, False)
+    assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, st, need, 256, *hp, 1) == zs.ZERO_E_RANK
+    assert zs.zero_stat(c, zs.ZERO_STAT_LAUNCHES) == 0 and zs.zero_stat(c, zs.ZERO_STAT_T) == 0
+    zs.zero_destroy(c)

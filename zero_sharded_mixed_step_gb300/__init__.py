@@ -50,6 +50,8 @@ SIGNATURES = {
     "zero_refresh_working_copy": (_I, [_P]),
     "zero_step": (_I, [_P, _I, _I, _L, _PP, _D, _D, _D, _D, _L]),
     "zero_set_unit_hook": (_I, [_P, HOOK, _P]),
+    "zero_host_staging_bytes": (_L, [_I, _I, _L, _LP, _L]),
+    "zero_step_host": (_I, [_P, _I, _I, _L, _PP, _P, _P, _L, _L, _D, _D, _D, _D, _L, _P, _P]),
     "zero_gather_unit": (_I, [_P, _L, _P, _P]),
     "zero_release_unit": (_I, [_P, _L]),
     "zero_update_unit": (_I, [_P, _L, _PP, _D, _D, _D, _D, _L, _P]),
@@ -176,6 +178,19 @@ def zero_refresh_working_copy(ctx) -> None:
 
 def zero_step(ctx, scheme, W, n, grads, lr, beta1, beta2, eps, t) -> None:
     _check("zero_step", lib().zero_step(ctx, scheme, W, n, _ptr_array(grads), lr, beta1, beta2, eps, t))
+
+
+def zero_host_staging_bytes(scheme, W, unit_sizes, chunk_elems=0) -> int:
+    return _check("zero_host_staging_bytes", lib().zero_host_staging_bytes(
+        scheme, W, len(unit_sizes), _i64_array(unit_sizes), chunk_elems))
+
+
+def zero_step_host(ctx, scheme, W, n, host_grads, host_out, staging, staging_bytes, chunk_elems,
+                   lr, beta1, beta2, eps, t, stream_h2d=None, stream_d2h=None) -> None:
+    """host_grads: W host buffers (tensors or addresses); host_out: host buffer or None."""
+    _check("zero_step_host", lib().zero_step_host(
+        ctx, scheme, W, n, _ptr_array(host_grads), _ptr(host_out), _ptr(staging), staging_bytes, chunk_elems,
+        lr, beta1, beta2, eps, t, _stream(stream_h2d), _stream(stream_d2h)))
 
 
 def zero_set_unit_hook(ctx, fn, user=None):
