@@ -219,6 +219,29 @@ int zero_step(zero_ctx* ctx, int scheme, int W, int64_t n, const void* const* gr
 /* Register (fn != NULL) or clear the ZeRO-3 unit hook. */
 int zero_set_unit_hook(zero_ctx* ctx, zero_unit_hook fn, void* user);
 
+/* ---- the step bucket by bucket --------------------------------------------- */
+
+/*
+ * One bucket of a DP/Z1/Z2 step: reduce-scatter (mean) + Adam + recast of
+ * the flat range [lo, lo + len), as soon as the ranks' gradients for that
+ * range exist ("ZeRO and FSDP": real ZeRO-2 reduce-scatters by bucket during
+ * the backward pass; "One Poem Suffices: ZeRO" section 4.2.2: constant-size
+ * buffers).  The update is elementwise, so a step done bucket by bucket is
+ * bit-identical to zero_step, and the full gradient vectors never need to
+ * exist: bucket_grads[w] points at rank w's len gradient values of the range
+ * (device, 16-byte aligned; lo must be a multiple of 8).
+ *   t      the first bucket of a step passes the context's step counter + 1,
+ *          the others the same t.  A step's buckets may arrive in any order but
+ *          must cover [0, n_pad) exactly once before the next step (or any
+ *          other kind of step) starts: an overlap, or a new step while one is
+ *          incomplete, is ZERO_E_STATE.
+ *   stream cudaStream_t (NULL: the update stream).
+ * Traffic: the step's two collectives are counted when its last bucket
+ * arrives.  ZeRO-3 updates unit by unit with zero_update_unit instead.
+ */
+int zero_step_bucket(zero_ctx* ctx, int64_t lo, int64_t len, const void* const* bucket_grads, double lr,
+                     double beta1, double beta2, double eps, int64_t t, void* stream);
+
 /* ---- the step fed from host memory ---------------------------------------- */
 
 /*

@@ -230,3 +230,21 @@ def test_step_host_checks_before_any_launch(zlib):
     assert _err(zs.zero_step_host, c, 1, 4, 1000, hg, None, st, need, 256, *hp, 1) == zs.ZERO_E_RANK
     assert zs.zero_stat(c, zs.ZERO_STAT_LAUNCHES) == 0 and zs.zero_stat(c, zs.ZERO_STAT_T) == 0
     zs.zero_destroy(c)
+
+
+def test_step_bucket_checks_before_any_launch(zlib):
+    c = make_ctx(scheme=2, W=4, units=(1000,))
+    b = [fake(70 + r) for r in range(4)]
+    hp = (1e-3, 0.9, 0.999, 1e-8)
+    assert _err(zs.zero_step_bucket, c, 4, 16, b, *hp, 1) == zs.ZERO_E_ALIGN          # lo not a multiple of 8
+    assert _err(zs.zero_step_bucket, c, 0, 0, b, *hp, 1) == zs.ZERO_E_ARG             # empty
+    assert _err(zs.zero_step_bucket, c, 992, 16, b, *hp, 1) == zs.ZERO_E_ARG          # past n_pad
+    assert _err(zs.zero_step_bucket, c, 0, 16, b[:3] + [None], *hp, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_step_bucket, c, 0, 16, b[:3] + [fake(80) + 2], *hp, 1) == zs.ZERO_E_ALIGN
+    assert _err(zs.zero_step_bucket, c, 0, 16, b, *hp, 2) == zs.ZERO_E_STATE          # t must start the step
+    assert _err(zs.zero_step_bucket, c, 0, 16, b, *hp, 0) == zs.ZERO_E_STATE
+    assert zs.zero_stat(c, zs.ZERO_STAT_LAUNCHES) == 0
+    zs.zero_destroy(c)
+    d = make_ctx(scheme=3, W=4, units=(13, 24, 3))
+    assert _err(zs.zero_step_bucket, d, 0, 8, b, *hp, 1) == zs.ZERO_E_ARG             # ZeRO-3 goes unit by unit
+    zs.zero_destroy(d)

@@ -50,6 +50,7 @@ SIGNATURES = {
     "zero_refresh_working_copy": (_I, [_P]),
     "zero_step": (_I, [_P, _I, _I, _L, _PP, _D, _D, _D, _D, _L]),
     "zero_set_unit_hook": (_I, [_P, HOOK, _P]),
+    "zero_step_bucket": (_I, [_P, _L, _L, _PP, _D, _D, _D, _D, _L, _P]),
     "zero_host_staging_bytes": (_L, [_I, _I, _L, _LP, _L]),
     "zero_step_host": (_I, [_P, _I, _I, _L, _PP, _P, _P, _L, _L, _D, _D, _D, _D, _L, _P, _P]),
     "zero_gather_unit": (_I, [_P, _L, _P, _P]),
@@ -178,6 +179,11 @@ def zero_refresh_working_copy(ctx) -> None:
 
 def zero_step(ctx, scheme, W, n, grads, lr, beta1, beta2, eps, t) -> None:
     _check("zero_step", lib().zero_step(ctx, scheme, W, n, _ptr_array(grads), lr, beta1, beta2, eps, t))
+
+
+def zero_step_bucket(ctx, lo, length, bucket_grads, lr, beta1, beta2, eps, t, stream=None) -> None:
+    _check("zero_step_bucket", lib().zero_step_bucket(ctx, lo, length, _ptr_array(bucket_grads), lr, beta1, beta2, eps,
+                                                      t, _stream(stream)))
 
 
 def zero_host_staging_bytes(scheme, W, unit_sizes, chunk_elems=0) -> int:

@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <string>
 #include <thread>
 #include <vector>
@@ -149,6 +150,10 @@ struct zero_ctx {
   bool err_slot_ready = false; // cleared on the device (at the first fused launch)
   int64_t dev_err_seen = 0;    // count at the last zero_sync
   int last_variant = 0;
+  // a step being done bucket by bucket: the ranges covered so far (lo -> hi)
+  bool bucket_open = false;
+  std::map<int64_t, int64_t> covered;
+  int64_t covered_elems = 0;
   std::vector<cudaEvent_t> event_pool;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[3];
 };
@@ -220,6 +225,14 @@ int check_grads(const zero_ctx* c, const void* const* grads) {
     if (grads[w] == nullptr && c->L.n_pad > 0) return fail(ZERO_E_ARG, "gradient pointer of rank %d is NULL", w);
     if (!aligned16(grads[w])) return fail(ZERO_E_ALIGN, "gradient pointer of rank %d is not 16-byte aligned", w);
   }
+  return ZERO_OK;
+}
+
+// A step done bucket by bucket must be complete before any other step starts.
+int check_no_open_bucket_step(const zero_ctx* c) {
+  if (c->bucket_open)
+    return fail(ZERO_E_STATE, "step %lld is being done bucket by bucket and %lld of %lld elements are still missing",
+                (long long)c->t, (long long)(c->L.n_pad - c->covered_elems), (long long)c->L.n_pad);
   return ZERO_OK;
 }
 
@@ -716,6 +729,7 @@ int zero_step(zero_ctx* c, int scheme, int W, int64_t n, const void* const* grad
   if (rc) return rc;
   if (t != c->t + 1)
     return fail(ZERO_E_STATE, "step counter %lld does not follow %lld", (long long)t, (long long)c->t);
+  if ((rc = check_no_open_bucket_step(c))) return rc;
   if ((rc = check_grads(c, grads)) || (rc = check_ranks_up(c))) return rc;
   for (size_t u = 0; u < c->live.size(); ++u)
     if (c->live[u]) return fail(ZERO_E_STATE, "unit %zu is still gathered by the caller", u);
@@ -760,6 +774,7 @@ int zero_step_host(zero_ctx* c, int scheme, int W, int64_t n, const void* const*
   if (t != c->t + 1)
     return fail(ZERO_E_STATE, "step counter %lld does not follow %lld", (long long)t, (long long)c->t);
   if (chunk_elems < 0 || chunk_elems > (int64_t(1) << 40)) return fail(ZERO_E_ARG, "chunk_elems out of range");
+  if ((rc = check_no_open_bucket_step(c))) return rc;
   if (host_grads == nullptr) return fail(ZERO_E_ARG, "host_grads is NULL");
   for (int w = 0; w < W; ++w)
     if (host_grads[w] == nullptr && c->L.n_pad > 0) return fail(ZERO_E_ARG, "host gradients of rank %d are NULL", w);
@@ -784,6 +799,78 @@ int zero_step_host(zero_ctx* c, int scheme, int W, int64_t n, const void* const*
     if (rc) return rc;
   }
   c->t = t;
+  return ZERO_OK;
+}
+
+int zero_step_bucket(zero_ctx* c, int64_t lo, int64_t len, const void* const* bucket_grads, double lr,
+                     double beta1, double beta2, double eps, int64_t t, void* stream) {
+  if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
+  if (c->scheme == ZERO_SCHEME_Z3) return fail(ZERO_E_ARG, "ZeRO-3 updates unit by unit: use zero_update_unit");
+  int rc = check_hyper(lr, beta1, beta2, eps, t);
+  if (rc) return rc;
+  if (len <= 0 || lo < 0 || lo > c->L.n_pad - len)
+    return fail(ZERO_E_ARG, "bucket [%lld, %lld) is not inside [0, %lld)", (long long)lo, (long long)(lo + len),
+                (long long)c->L.n_pad);
+  if (lo % 8 != 0) return fail(ZERO_E_ALIGN, "a bucket must start at a multiple of 8 elements (lo=%lld)", (long long)lo);
+  if (bucket_grads == nullptr) return fail(ZERO_E_ARG, "bucket_grads is NULL");
+  for (int w = 0; w < c->W; ++w) {
+    if (bucket_grads[w] == nullptr) return fail(ZERO_E_ARG, "bucket of rank %d is NULL", w);
+    if (!aligned16(bucket_grads[w])) return fail(ZERO_E_ALIGN, "bucket of rank %d is not 16-byte aligned", w);
+  }
+  const bool new_step = t == c->t + 1;
+  if (new_step) {
+    if ((rc = check_no_open_bucket_step(c))) return rc;
+  } else if (!(t == c->t && c->bucket_open)) {
+    return fail(ZERO_E_STATE, "bucket of step %lld: the context is at step %lld%s", (long long)t, (long long)c->t,
+                c->bucket_open ? "" : " and no bucketed step is open");
+  }
+  if (!new_step) {
+    // no overlap with what this step has already covered
+    auto it = c->covered.upper_bound(lo);
+    if (it != c->covered.end() && it->first < lo + len)
+      return fail(ZERO_E_STATE, "bucket [%lld, %lld) overlaps one already applied in step %lld", (long long)lo,
+                  (long long)(lo + len), (long long)t);
+    if (it != c->covered.begin() && std::prev(it)->second > lo)
+      return fail(ZERO_E_STATE, "bucket [%lld, %lld) overlaps one already applied in step %lld", (long long)lo,
+                  (long long)(lo + len), (long long)t);
+  }
+  if ((rc = check_ranks_up(c))) return rc;
+  for (size_t u = 0; u < c->live.size(); ++u)
+    if (c->live[u]) return fail(ZERO_E_STATE, "unit %zu is still gathered by the caller", u);
+  // the kernel indexes gradients by flat position: shift each bucket back by lo
+  const void* g[zero::kMaxRanks];
+  for (int w = 0; w < c->W; ++w) g[w] = static_cast<const char*>(bucket_grads[w]) - lo * 2;
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : c->su;
+  rc = launch_update(c, 0, g, make_coef(lr, beta1, beta2, eps, t, c->W), s, nullptr, lo, len);
+  if (rc) return rc;
+  if (new_step) {
+    c->covered.clear();
+    c->covered_elems = 0;
+    c->bucket_open = true;
+    c->t = t;
+  }
+  // record [lo, lo + len), merging with its neighbours
+  int64_t a = lo, b = lo + len;
+  auto it = c->covered.lower_bound(a);
+  if (it != c->covered.begin() && std::prev(it)->second == a) {
+    --it;
+    a = it->first;
+    it = c->covered.erase(it);
+  }
+  if (it != c->covered.end() && it->first == b) {
+    b = it->second;
+    c->covered.erase(it);
+  }
+  c->covered[a] = b;
+  c->covered_elems += len;
+  if (c->covered_elems == c->L.n_pad) {
+    // the whole vector is done: the step's reduce-scatter and all-gather
+    c->bucket_open = false;
+    c->covered.clear();
+    count_scatter(c, 0);
+    c->gathers += 1;
+    c->comm += ring_bytes(c->W, c->L.shard[0]);
+  }
   return ZERO_OK;
 }
 
@@ -857,6 +944,7 @@ int zero_get_state(zero_ctx* c, float* master, float* m, float* v, int64_t* t) {
 
 int zero_set_state(zero_ctx* c, const float* master, const float* m, const float* v, int64_t t) {
   if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
+  if (int rb = check_no_open_bucket_step(c)) return rb;
   if (!master || !m || !v) return fail(ZERO_E_ARG, "master, m and v are required");
   if (t < 0) return fail(ZERO_E_ARG, "step counter must be >= 0");
   int rc = zero_sync(c, -1);
