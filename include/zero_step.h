@@ -357,6 +357,18 @@ int zero_enable_timing(zero_ctx* ctx, int on);
  */
 int zero_read_timing(zero_ctx* ctx, int kernel, double* total_ms, int64_t* launches);
 
+/* ---- debugging ----------------------------------------------------------------- */
+#define ZERO_DEBUG_POISON_RELEASED 1  /* fill a released ZeRO-3 unit buffer with NaN */
+
+/*
+ * Debug flags (ZERO_DEBUG_*, or 0).  With ZERO_DEBUG_POISON_RELEASED, every
+ * ZeRO-3 unit buffer is filled with the 16-bit NaN 0x7FFF when its unit is
+ * released (zero_release_unit, and each release inside zero_step), in order
+ * on the stream that used it: work that reads a unit after its release then
+ * sees NaN instead of plausible stale weights.  Costs one fill per release.
+ */
+int zero_set_debug(zero_ctx* ctx, int flags);
+
 /*
  * Select the fused-pass variant (ZERO_VARIANT_*).  AUTO uses the bulk-staged
  * kernel where it measured faster (W of 8 or 16, at least one 2048-element

@@ -213,3 +213,54 @@ def test_bounded_device_wait_reports_and_recovers():
     s.sync(timeout_ms=60_000)
     assert s.stat(zs.ZERO_STAT_DEVICE_ERRORS) == 1
     s.close()
+
+
+def test_poison_released_units():
+    """With ZERO_DEBUG_POISON_RELEASED a released unit buffer holds NaN
+    (0x7FFF), both through the caller-driven API and inside zero_step, while
+    everything read before the release, and the step's results, are unchanged."""
+    units = [4096 * 3 + 5, 70_001]
+    W = 8
+    wl = wk.scaled(wk.LAYER_UNITS, unit_sizes=units, steps=2, name="poison")
+    theta0 = wk.draw_theta0(wl, "cuda")
+    plain = zs.ZeroStep(zs.ZERO_SCHEME_Z3, W, units, "bf16", theta0=theta0)
+    s = zs.ZeroStep(zs.ZERO_SCHEME_Z3, W, units, "bf16", theta0=theta0)
+    s.set_debug(zs.ZERO_DEBUG_POISON_RELEASED)
+    grads = _grads(wl, "bf16", 2, s)
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    # caller-driven: gather, check, release, check the poison
+    buf = torch.zeros(s.sizes["unit_buf"], dtype=torch.bfloat16, device="cuda")
+    n0 = s.shard[0] * W
+    zs.zero_gather_unit(s.ctx, 0, buf)
+    torch.cuda.synchronize()
+    assert torch.equal(buf[:n0], s.working_copy()[:n0])
+    zs.zero_release_unit(s.ctx, 0)
+    torch.cuda.synchronize()
+    assert bool((buf[:n0].view(torch.int16) == 0x7FFF).all())
+    # inside zero_step: what the hook reads comes before the release
+    seen = []
+
+    def hook(_user, phase, unit, ptr, stream):
+        st = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
+        with torch.cuda.stream(st):
+            b = next(x for x in s.unit_bufs if x.data_ptr() == ptr)
+            seen.append((unit, b[: s.shard[unit] * W].clone()))
+
+    s.set_unit_hook(hook)
+    before = s.working_copy().clone()
+    s.step(grads[0], *hp, 1)
+    plain.set_unit_hook(lambda *a: None)
+    plain.step(grads[0], *hp, 1)
+    torch.cuda.synchronize()
+    for unit, vals in seen:
+        o = s.off[unit]
+        assert torch.equal(vals, before[o:o + vals.numel()])
+    for b in s.unit_bufs:
+        assert bool((b.view(torch.int16) == 0x7FFF).all())
+    for x, y in ((plain.master, s.master), (plain.m, s.m), (plain.v, s.v)):
+        assert torch.equal(x, y)
+    assert torch.equal(plain.working_copy(), s.working_copy())
+    with pytest.raises(zs.ZeroError):
+        zs.zero_set_debug(s.ctx, 8)
+    plain.close()
+    s.close()

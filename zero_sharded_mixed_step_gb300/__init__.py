@@ -31,6 +31,7 @@ ZERO_VARIANT_AUTO, ZERO_VARIANT_VECTOR, ZERO_VARIANT_BULK = 0, 1, 2
  ZERO_STAT_PEAK_LIVE_ELEMS, ZERO_STAT_T, ZERO_STAT_DEVICE_ERRORS, ZERO_STAT_LAST_VARIANT) = range(9)
 ZERO_MAX_RANKS = 64
 ZERO_KERNEL_FUSED, ZERO_KERNEL_GATHER, ZERO_KERNEL_CAST = 0, 1, 2
+ZERO_DEBUG_POISON_RELEASED = 1
 
 ERROR_NAMES = {ZERO_E_ARG: "ZERO_E_ARG", ZERO_E_ALIGN: "ZERO_E_ALIGN", ZERO_E_CUDA: "ZERO_E_CUDA",
                ZERO_E_RANK: "ZERO_E_RANK", ZERO_E_TIMEOUT: "ZERO_E_TIMEOUT", ZERO_E_STATE: "ZERO_E_STATE"}
@@ -65,6 +66,7 @@ SIGNATURES = {
     "zero_read_timing": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _LP]),
     "zero_set_variant": (_I, [_P, _I]),
     "zero_inject_stall": (_I, [_P, _L]),
+    "zero_set_debug": (_I, [_P, _I]),
     "zero_mark_rank": (_I, [_P, _I, _I]),
     "zero_step_z3_static": (_I, [_I, _L, _LP, _I, _I, _P, _P, _P, _PP, _PP, _D, _D, _D, _D, _L, HOOK, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
@@ -257,6 +259,10 @@ def zero_set_variant(ctx, variant: int) -> None:
     _check("zero_set_variant", lib().zero_set_variant(ctx, variant))
 
 
+def zero_set_debug(ctx, flags: int) -> None:
+    _check("zero_set_debug", lib().zero_set_debug(ctx, flags))
+
+
 def zero_inject_stall(ctx, tile: int) -> None:
     _check("zero_inject_stall", lib().zero_inject_stall(ctx, tile))
 
@@ -362,6 +368,9 @@ class ZeroStep:
 
     def set_variant(self, variant):
         zero_set_variant(self.ctx, variant)
+
+    def set_debug(self, flags):
+        zero_set_debug(self.ctx, flags)
 
     def stat(self, which):
         return zero_stat(self.ctx, which)

@@ -100,7 +100,22 @@ dim3 grid_for(const CopySeg* segs, int nseg, int64_t per_thread) {
   return dim3(static_cast<unsigned>(bx), static_cast<unsigned>(nseg));
 }
 
+__global__ void __launch_bounds__(kCopyThreads) fill16(uint16_t* dst, int64_t n, uint16_t value) {
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n; k += nthreads) dst[k] = value;
+}
+
 }  // namespace
+
+cudaError_t launch_fill16(void* dst, int64_t count, uint16_t value, cudaStream_t stream, int64_t* launches) {
+  if (count <= 0) return cudaSuccess;
+  int64_t blocks = (count + kCopyThreads - 1) / kCopyThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  fill16<<<static_cast<unsigned>(blocks), kCopyThreads, 0, stream>>>(static_cast<uint16_t*>(dst), count, value);
+  ++*launches;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int64_t* launches) {
   if (nseg <= 0) return cudaSuccess;

@@ -5,6 +5,7 @@
 #include "zero_step.h"
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <chrono>
 #include <cmath>
@@ -45,6 +46,21 @@ int cuda_fail(cudaError_t e, const char* what) {
     cudaError_t e_ = (call);                            \
     if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
   } while (0)
+
+// NVTX range on the host timeline (a no-op unless a profiler is attached)
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  Range(const char* fmt, long long a) {
+    char buf[96];
+    snprintf(buf, sizeof buf, fmt, a);
+    nvtxRangePushA(buf);
+  }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
+constexpr uint16_t kPoison16 = 0x7FFF;   // a NaN in both fp16 and bf16
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // master, m and v are read and written 32 bytes at a time
@@ -151,6 +167,9 @@ struct zero_ctx {
   int64_t dev_err_seen = 0;    // count at the last zero_sync
   int last_variant = 0;
   // a step being done bucket by bucket: the ranges covered so far (lo -> hi)
+  int debug = 0;
+  std::vector<void*> live_buf;          // where the caller gathered each live unit
+  std::vector<cudaStream_t> live_stream;
   bool bucket_open = false;
   std::map<int64_t, int64_t> covered;
   int64_t covered_elems = 0;
@@ -348,6 +367,13 @@ void live_add(zero_ctx* c, int64_t elems) {
   if (c->live_elems > c->peak_live) c->peak_live = c->live_elems;
 }
 
+int poison_unit(zero_ctx* c, int64_t u, void* buf, cudaStream_t s) {
+  if (!(c->debug & ZERO_DEBUG_POISON_RELEASED)) return ZERO_OK;
+  cudaError_t e = zero::launch_fill16(buf, c->L.shard[u] * c->W, kPoison16, s, &c->launches);
+  if (e != cudaSuccess) return cuda_fail(e, "poisoning a released unit");
+  return ZERO_OK;
+}
+
 // ZeRO-3 step: forward gathers in unit order, backward gathers in reverse
 // order each followed by the unit's update, two gather buffers in turn.  The
 // gather of the next unit (stream G) waits only for the buffer it reuses to
@@ -374,6 +400,7 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
   int64_t held[2] = {0, 0};
   int64_t seq = 0;
   auto unit = [&](int64_t u, int phase) -> int {
+    Range range(phase == 0 ? "zero3 forward unit %lld" : "zero3 backward unit %lld", static_cast<long long>(u));
     const int b = static_cast<int>(seq++ & 1);
     void* buf = c->ubuf[b];
     if (used[b] && two_streams) ZERO_CUDA(cudaStreamWaitEvent(sg, c->ev_free[b], 0));
@@ -388,6 +415,7 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
       r = launch_update(c, u, grads, coef, su, buf);
       if (r) return r;
       count_scatter(c, u);
+      if ((r = poison_unit(c, u, buf, su))) return r;
       used[b] = true;
       return ZERO_OK;
     }
@@ -403,6 +431,7 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
       if (r) return r;
       count_scatter(c, u);
     }
+    if ((r = poison_unit(c, u, buf, su))) return r;
     if (two_streams) ZERO_CUDA(cudaEventRecord(c->ev_free[b], su));
     used[b] = true;
     return ZERO_OK;
@@ -657,6 +686,8 @@ int zero_init(zero_ctx** out, int scheme, int W, int64_t n, int64_t n_units, con
   c->su = static_cast<cudaStream_t>(stream_update);
   c->sg = stream_gather ? static_cast<cudaStream_t>(stream_gather) : c->su;
   c->live.assign(static_cast<size_t>(n_units), 0);
+  c->live_buf.assign(static_cast<size_t>(n_units), nullptr);
+  c->live_stream.assign(static_cast<size_t>(n_units), nullptr);
   c->rank_up.assign(static_cast<size_t>(W), 1);
   c->err_slot = take_slot();
   *out = c;
@@ -734,6 +765,7 @@ int zero_step(zero_ctx* c, int scheme, int W, int64_t n, const void* const* grad
   for (size_t u = 0; u < c->live.size(); ++u)
     if (c->live[u]) return fail(ZERO_E_STATE, "unit %zu is still gathered by the caller", u);
   const zero::AdamCoef coef = make_coef(lr, beta1, beta2, eps, t, W);
+  Range range("zero_step %lld", static_cast<long long>(t));
   if (c->scheme != ZERO_SCHEME_Z3) {
     rc = launch_update(c, 0, grads, coef, c->su);
     if (rc) return rc;
@@ -794,6 +826,7 @@ int zero_step_host(zero_ctx* c, int scheme, int W, int64_t n, const void* const*
   const zero::AdamCoef coef = make_coef(lr, beta1, beta2, eps, t, W);
   cudaStream_t sh = stream_h2d ? static_cast<cudaStream_t>(stream_h2d) : c->su;
   cudaStream_t sd = stream_d2h ? static_cast<cudaStream_t>(stream_d2h) : c->su;
+  Range range("zero_step_host %lld", static_cast<long long>(t));
   if (c->L.n_pad > 0) {
     rc = run_host_step(c, host_grads, host_out, static_cast<char*>(staging), chunk, slot, coef, sh, sd);
     if (rc) return rc;
@@ -894,6 +927,8 @@ int zero_gather_unit(zero_ctx* c, int64_t unit, void* dst, void* stream) {
   rc = launch_gather(c, unit, dst, s);
   if (rc) return rc;
   c->live[unit] = 1;
+  c->live_buf[unit] = dst;
+  c->live_stream[unit] = s;
   live_add(c, c->L.shard[unit] * c->W);
   count_gather(c, unit);
   return ZERO_OK;
@@ -905,6 +940,8 @@ int zero_release_unit(zero_ctx* c, int64_t unit) {
   if (unit < 0 || unit >= static_cast<int64_t>(c->L.size.size()))
     return fail(ZERO_E_ARG, "unit %lld out of range", (long long)unit);
   if (!c->live[unit]) return fail(ZERO_E_STATE, "unit %lld is not gathered", (long long)unit);
+  int rc = poison_unit(c, unit, c->live_buf[unit], c->live_stream[unit]);
+  if (rc) return rc;
   c->live[unit] = 0;
   c->live_elems -= c->L.shard[unit] * c->W;
   return ZERO_OK;
@@ -1069,6 +1106,13 @@ int zero_set_variant(zero_ctx* c, int variant) {
   if (variant != ZERO_VARIANT_AUTO && variant != ZERO_VARIANT_VECTOR && variant != ZERO_VARIANT_BULK)
     return fail(ZERO_E_ARG, "unknown variant %d", variant);
   c->variant = variant;
+  return ZERO_OK;
+}
+
+int zero_set_debug(zero_ctx* c, int flags) {
+  if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
+  if (flags & ~ZERO_DEBUG_POISON_RELEASED) return fail(ZERO_E_ARG, "unknown debug flags %d", flags);
+  c->debug = flags;
   return ZERO_OK;
 }
 

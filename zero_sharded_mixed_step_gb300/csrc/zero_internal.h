@@ -74,6 +74,9 @@ cudaError_t launch_fused_step(const FusedLaunch& a, cudaStream_t stream, int64_t
 // Gather: copy each segment's bytes (16-byte vectors where both ends allow).
 cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int64_t* launches);
 
+// Fill count 16-bit values with `value` (debug poisoning of released units).
+cudaError_t launch_fill16(void* dst, int64_t count, uint16_t value, cudaStream_t stream, int64_t* launches);
+
 // Cast fp32 -> 16-bit (round to nearest even) for each segment.
 cudaError_t launch_cast(const CopySeg* segs, int nseg, int work_dtype, cudaStream_t stream, int64_t* launches);
 
