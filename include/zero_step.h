@@ -170,9 +170,12 @@ int64_t zero_comm_bytes_closed_form(int scheme, int64_t n, int W);
  *                     uses for ZeRO-3 (Z3; NULL otherwise).
  *   stream_update     cudaStream_t for updates (may be the caller's stream;
  *                     NULL means the legacy default stream).
- *   stream_gather     cudaStream_t for ZeRO-3 gathers, so that the next
- *                     unit's gather overlaps the current update; NULL means
- *                     stream_update (no overlap).
+ *   stream_gather     cudaStream_t for ZeRO-3 gathers, so that with a unit
+ *                     hook the next unit's gather overlaps the work on the
+ *                     current one; NULL means stream_update (no overlap).
+ *                     Work the caller enqueues on different streams itself
+ *                     (zero_gather_unit, zero_update_unit) is ordered by the
+ *                     caller.
  * On success *out receives the context.  Call zero_refresh_working_copy
  * once after writing theta0, before the first step or gather.
  */
