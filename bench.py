@@ -424,7 +424,11 @@ def run_ours(args):
     # pipelined chunk by chunk (unit by unit for ZeRO-3) on three streams.
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
-        host_grads = [g.to("cpu").pin_memory() for g in step.grads]
+        host_grads = []
+        for g in step.grads:                     # straight into pinned memory, no pageable copy
+            h = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+            h.copy_(g)
+            host_grads.append(h)
         out_elems = step.n_pad if scheme != 3 else wl.W * step.sizes["shard_store"]
         host_out = torch.empty(out_elems, dtype=step.work_torch_dtype, pin_memory=True)
         need = zs.zero_host_staging_bytes(scheme, wl.W, units, 0)
