@@ -54,7 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="zero3_24x50m_w8",
-                   choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1"])
+                   choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1",
+                            "gpt2_small_124m_w8_dp_replicas"])
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None)
     p.add_argument("--params", type=int, default=None,
                    help="flat workloads only: a smaller copy with this many parameters (same W, dtype, "
@@ -95,12 +96,19 @@ def layout_sizes(wl):
     return sum(padded), padded, units
 
 
+def bytes_per_element(wl):
+    """Bytes the fused pass moves per element: the W 16-bit gradients read
+    once, then 12 read + 14 written per copy of the state (W copies when the
+    DP replicas are kept literally)."""
+    return 2 * wl.W + 26 * (wl.W if wl.dp_replicas else 1)
+
+
 def algorithmic_bytes(wl):
-    """Bytes a step must move: the fused pass reads 2 W + 12 and writes 14
-    bytes per element; each ZeRO-3 gather reads and writes 2 bytes per
-    element, twice per step."""
+    """Bytes a step must move: the fused pass (bytes_per_element per
+    element); each ZeRO-3 gather reads and writes 2 bytes per element, twice
+    per step."""
     n_pad, _, _ = layout_sizes(wl)
-    fused = (2 * wl.W + 26) * n_pad
+    fused = bytes_per_element(wl) * n_pad
     gathers = 8 * n_pad if scheme_of(wl) == 3 else 0
     return fused, gathers
 
@@ -116,10 +124,11 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(kernel_file: str, workload_name: str):
-    """Per-launch DRAM bytes from the committed ncu summary of this kernel and
-    workload, or None when there is none or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"fused_step_{workload_name}.md")
+def recorded_traffic(profile: str, kernel_sources):
+    """Per-launch DRAM bytes from the committed ncu summary ``profiles/<profile>.md``,
+    or None when there is none or the kernel's sources (the files named, in
+    order) changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{profile}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -127,10 +136,20 @@ def recorded_traffic(kernel_file: str, workload_name: str):
     m2 = re.search(r"kernel_source_sha256\s*=\s*([0-9a-f]{64})", text)
     if not (m1 and m2):
         return None
-    src = open(os.path.join(ROOT, "zero_sharded_mixed_step_gb300", "csrc", kernel_file), "rb").read()
-    if hashlib.sha256(src).hexdigest() != m2.group(1):
+    if kernel_source_sha256(kernel_sources) != m2.group(1):
         return None
     return int(m1.group(1))
+
+
+def kernel_source_sha256(kernel_sources) -> str:
+    h = hashlib.sha256()
+    for name in kernel_sources:
+        h.update(open(os.path.join(ROOT, "zero_sharded_mixed_step_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
+FUSED_SOURCES = ("fused_step.cu", "step_math.cuh")
+REPLICA_SOURCES = ("dp_replicas.cu", "step_math.cuh")
 
 
 class ClockSampler:
@@ -284,7 +303,8 @@ def config_of(wl, dtype, gpus):
     n_pad, per_launch, units = layout_sizes(wl)
     fused, gathers = algorithmic_bytes(wl)
     names = {0: "data parallel", 1: "ZeRO-1", 2: "ZeRO-2", 3: "ZeRO-3"}
-    return {"workload": wl.name, "scheme": names[scheme_of(wl)], "W": wl.W, "params": wl.n, "padded": n_pad,
+    scheme = names[scheme_of(wl)] + (f", {wl.W} replicas kept literally" if wl.dp_replicas else "")
+    return {"workload": wl.name, "scheme": scheme, "W": wl.W, "params": wl.n, "padded": n_pad,
             "units": len(units), "grad_dtype": dtype, "work_dtype": dtype, "master_dtype": "f32",
             "algorithmic_bytes_per_step": fused + gathers,
             "l2": f"inputs larger than L2: {(fused + gathers) / 1e9:.1f} GB touched per step vs "
@@ -335,6 +355,8 @@ def run_ours(args):
 
     wl = workload(args.workload, args.units, args.params)
     dtype = args.dtype or wl.dtypes[0]
+    if wl.dp_replicas:
+        return run_replicas(args, wl, dtype, world, rank, dev)
     scheme = scheme_of(wl)
     n_pad, per_launch, units = layout_sizes(wl)
     su = torch.cuda.Stream(dev)
@@ -360,8 +382,7 @@ def run_ours(args):
     # CUDA event pair recorded around every kernel launch on its own stream
     # (zero_enable_timing) for the per-launch roofline; the brackets cost
     # about 3% of a ZeRO-3 step, so they stay out of pass 1.
-    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
-    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
+    gpu_id = gpu_uuid(dev)
 
     def timed_pass(instrumented: bool):
         nonlocal t
@@ -405,7 +426,7 @@ def run_ours(args):
     fused_avg_ms = fused_ms / max(1, fused_n)
     achieved = per_launch_bytes / (fused_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": recorded_traffic("fused_step.cu", wl.name),
+                "traffic": recorded_traffic(f"fused_step_{wl.name}", FUSED_SOURCES),
                 "kernel": "fused_step_bulk" if last_variant == zs.ZERO_VARIANT_BULK else "fused_step_vector",
                 "peak_source": f"{peak_src} copy bandwidth", "launch_ms": fused_avg_ms,
                 "algorithmic_bytes_per_launch": per_launch_bytes, "bytes_per_element": per_elem,
@@ -471,6 +492,130 @@ def run_ours(args):
             "config": config_of(wl, dtype, world),
             "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
             "roofline": roofline, "gather": gather_info, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def gpu_uuid(dev):
+    import torch
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    return f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or dev.index)
+
+
+def run_replicas(args, wl, dtype, world, rank, dev):
+    """Plain data parallelism with the W replicas kept literally
+    (zero_step_dp_replicas): every rank's fp32 master, m, v and 16-bit copy
+    in HBM, one kernel per step that reads the W gradients once and updates
+    all W replicas.  The same line as the sharded workloads, for the cost
+    that sharding removes."""
+    import torch
+    import torch.distributed as dist
+    import zero_sharded_mixed_step_gb300 as zs
+    import workloads as wk
+
+    su = torch.cuda.Stream(dev)
+    with torch.cuda.stream(su):
+        theta0 = wk.draw_theta0(wl, dev)
+        rep = zs.DpReplicas(wl.W, wl.n, dtype, theta0=theta0, device=dev, stream=su)
+        del theta0
+        grads = rep.new_grad_buffers()
+        for g, d in zip(grads, wk.GradSource(wl, dtype, dev).step(1)):
+            g[: wl.n].copy_(d)
+            del d
+    torch.cuda.synchronize()
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        rep.step(grads, *hp, t)
+    torch.cuda.synchronize()
+
+    # timed region: inputs resident in HBM, one kernel launch per step on su,
+    # so the events around the loop time the launches themselves
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid(dev)) as clocks:
+        e0.record(su)
+        for _ in range(args.steps):
+            t += 1
+            rep.step(grads, *hp, t)
+        e1.record(su)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms_per_step = ms / args.steps
+    launches = args.steps
+    if rep.mismatches() != 0:
+        raise RuntimeError("the DP replicas drifted apart")
+    value = whole_job_value(world, wl.n, args.steps, ms)
+    per_elem = bytes_per_element(wl)
+    step_bytes = per_elem * rep.n_pad
+    peak, peak_src = hbm_peak()
+    achieved = step_bytes / (ms_per_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(f"dp_replicas_step_{wl.name}", REPLICA_SOURCES),
+                "kernel": "dp_replicas_step", "peak_source": f"{peak_src} copy bandwidth",
+                "launch_ms": ms_per_step, "algorithmic_bytes_per_launch": step_bytes,
+                "bytes_per_element": per_elem, "frac_of_8tbs_nominal": achieved / 8000.0, "launches_timed": launches}
+
+    # end to end: every step copies the W gradient vectors in from pinned
+    # host memory and reads replica 0's 16-bit working copy back
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        host_grads = []
+        for g in grads:
+            h = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+            h.copy_(g)
+            host_grads.append(h)
+        host_out = torch.empty(rep.n_pad, dtype=rep.work_torch_dtype, pin_memory=True)
+
+        def host_step():
+            nonlocal t
+            t += 1
+            with torch.cuda.stream(su):
+                for g, h in zip(grads, host_grads):
+                    g.copy_(h, non_blocking=True)
+                rep.step(grads, *hp, t)
+                host_out.copy_(rep.p16[0], non_blocking=True)
+
+        host_step()
+        su.synchronize()
+        if world > 1:
+            dist.barrier()
+        h0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            host_step()
+        su.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - h0)
+        e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
+               "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
+               "path": "pinned host gradients -> device gradient buffers (one copy per rank) -> "
+                       "zero_step_dp_replicas -> replica 0's 16-bit working copy -> pinned host, one stream"}
+        del host_grads, host_out
+
+    resident = sum(x.numel() * x.element_size() for x in rep.master + rep.m + rep.v + rep.p16)
+    del rep, grads
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, dtype, args.cpu_seconds)
+    if rank == 0:
+        config = config_of(wl, dtype, world)
+        config["replicated_state_bytes"] = resident
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+            "step_hbm_gbs": achieved, "step_frac_of_peak": achieved / peak,
+            "roofline": roofline, "gather": None, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks.summary(),
         }
         print(json.dumps(line))

@@ -437,6 +437,54 @@ int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_sizes, int g
                         double lr, double beta1, double beta2, double eps, int64_t t,
                         zero_unit_hook hook, void* user, void* stream);
 
+/* ---- data parallelism with literal replicas ---------------------------------- */
+
+/*
+ * One DP step with every rank's replica kept literally ("The four schemes":
+ * the DP baseline, every rank holding the 16-bit weights, the gradients and
+ * the fp32 master, m and v in full; "ZeRO, annotated": the redundancy the
+ * three ZeRO stages remove).  zero_step for ZERO_SCHEME_DP keeps one copy,
+ * since the replicas are equal by construction; this call materialises all
+ * W of them, to measure what sharding saves.
+ *   W, n          ranks (1..ZERO_MAX_RANKS) and real parameters; every vector
+ *                 holds n_pad = ceil(n / W) * W values (padded tail zero),
+ *                 as zero_buffer_sizes reports for ZERO_SCHEME_DP.
+ *   grad_dtype, work_dtype  ZERO_FP16 or ZERO_BF16.
+ *   grads         host array of W device pointers: rank w's gradients
+ *                 (16-byte aligned), read only.
+ *   master, m, v  host arrays of W device pointers: replica r's fp32 state
+ *                 (32-byte aligned), read and written in place.
+ *   p16           host array of W device pointers: replica r's 16-bit
+ *                 working copy (16-byte aligned), written.
+ *   lr, beta1, beta2, eps, t  as for zero_step; there is no context, so the
+ *                 caller keeps t (t >= 1, else ZERO_E_STATE).
+ *   stream        the CUDA stream the one kernel is enqueued on (NULL: the
+ *                 legacy default stream); returns without waiting.
+ * Every replica receives the rank-ordered mean of the W gradients and the
+ * same Adam step, so the replicas stay bit-identical to one another and to
+ * zero_step for DP on the same inputs.  Buffers stay the caller's.  Returns
+ * ZERO_E_ARG for a NULL pointer, a bad dtype or hyper-parameter, or replica
+ * buffers that overlap one another or a gradient vector; ZERO_E_ALIGN for a
+ * misaligned pointer; ZERO_E_CUDA if the launch fails.
+ */
+int zero_step_dp_replicas(int W, int64_t n, int grad_dtype, int work_dtype, const void* const* grads,
+                          float* const* master, float* const* m, float* const* v, void* const* p16,
+                          double lr, double beta1, double beta2, double eps, int64_t t, void* stream);
+
+/*
+ * The lab's DP assertion: count the (replica r >= 1, element e) pairs, over
+ * the n_pad values of each vector, where master, m, v or the 16-bit copy of
+ * replica r differs bitwise from replica 0.  Arguments as for
+ * zero_step_dp_replicas (pointers aligned to their element size);
+ * `mismatches` is one int64 of device memory (8-byte aligned, the
+ * caller's), set to 0 and then to the count by work enqueued on `stream`;
+ * read it after that work finishes.  Returns ZERO_E_ARG / ZERO_E_ALIGN /
+ * ZERO_E_CUDA as above.
+ */
+int zero_dp_replicas_mismatches(int W, int64_t n, const float* const* master, const float* const* m,
+                                const float* const* v, const void* const* p16, int64_t* mismatches,
+                                void* stream);
+
 /* Message for the calling thread's last error ("" if none). */
 const char* zero_last_error(void);
 

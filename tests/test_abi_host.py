@@ -248,3 +248,38 @@ def test_step_bucket_checks_before_any_launch(zlib):
     d = make_ctx(scheme=3, W=4, units=(13, 24, 3))
     assert _err(zs.zero_step_bucket, d, 0, 8, b, *hp, 1) == zs.ZERO_E_ARG             # ZeRO-3 goes unit by unit
     zs.zero_destroy(d)
+
+
+def test_dp_replicas_checks_before_any_launch(zlib):
+    """The replica step and the replica check refuse bad arguments before
+    touching the GPU (fake addresses, no device needed)."""
+    W, n = 3, 1001
+    g = [fake(100 + r) for r in range(W)]
+    th, m, v, p = ([fake(200 + 10 * k + r) for r in range(W)] for k in range(4))
+    hp = (1e-3, 0.9, 0.999, 1e-8)
+    step = zs.zero_step_dp_replicas
+    assert _err(step, 0, n, 0, 0, g, th, m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(step, 65, n, 0, 0, g, th, m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, -1, 0, 0, g, th, m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, n, 2, 0, g, th, m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, n, 0, 0, g, th, m, v, p, *hp, 0) == zs.ZERO_E_STATE
+    assert _err(step, W, n, 0, 0, g, th, m, v, p, 1e-3, 1.0, 0.999, 1e-8, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, n, 0, 0, g, th, m, v, p, 1e-3, 0.9, 0.999, 0.0, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, n, 0, 0, g, None, m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, n, 0, 0, g, th[:2] + [None], m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert _err(step, W, n, 0, 0, g, th, m[:1] + [m[1] + 16] + m[2:], v, p, *hp, 1) == zs.ZERO_E_ALIGN
+    assert _err(step, W, n, 0, 0, g, th, m, v, p[:2] + [p[2] + 2], *hp, 1) == zs.ZERO_E_ALIGN
+    assert _err(step, W, n, 0, 0, [g[0] + 8] + g[1:], th, m, v, p, *hp, 1) == zs.ZERO_E_ALIGN
+    # replicas that share memory would be updated twice
+    assert _err(step, W, n, 0, 0, g, th, m, [v[0], v[0], v[2]], p, *hp, 1) == zs.ZERO_E_ARG
+    assert "overlap" in zs.zero_last_error()
+    assert _err(step, W, n, 0, 0, g, th, m, v, [p[0], th[1] + 1024, p[2]], *hp, 1) == zs.ZERO_E_ARG
+    # a gradient vector inside a replica buffer
+    assert _err(step, W, n, 0, 0, [g[0], th[2] + 32, g[2]], th, m, v, p, *hp, 1) == zs.ZERO_E_ARG
+    assert "gradient" in zs.zero_last_error()
+    check = zs.zero_dp_replicas_mismatches
+    assert _err(check, 0, n, th, m, v, p, fake(300)) == zs.ZERO_E_ARG
+    assert _err(check, W, n, th, m, v, p, None) == zs.ZERO_E_ARG
+    assert _err(check, W, n, th, m, v, p, fake(300) + 4) == zs.ZERO_E_ALIGN
+    assert _err(check, W, n, th, m, None, p, fake(300)) == zs.ZERO_E_ARG
+    assert _err(check, W, n, th, m, v, p[:2] + [p[2] + 1], fake(300)) == zs.ZERO_E_ALIGN

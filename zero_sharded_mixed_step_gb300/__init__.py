@@ -69,6 +69,8 @@ SIGNATURES = {
     "zero_set_debug": (_I, [_P, _I]),
     "zero_mark_rank": (_I, [_P, _I, _I]),
     "zero_step_z3_static": (_I, [_I, _L, _LP, _I, _I, _P, _P, _P, _PP, _PP, _D, _D, _D, _D, _L, HOOK, _P, _P]),
+    "zero_step_dp_replicas": (_I, [_I, _L, _I, _I, _PP, _PP, _PP, _PP, _PP, _D, _D, _D, _D, _L, _P]),
+    "zero_dp_replicas_mismatches": (_I, [_I, _L, _PP, _PP, _PP, _PP, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 
@@ -282,7 +284,24 @@ def zero_step_z3_static(W, unit_sizes, grad_dtype, work_dtype, master, m, v, sha
         _ptr_array(shard16), _ptr_array(grads), lr, beta1, beta2, eps, t, cb, None, _stream(stream)))
 
 
-# ---- convenience owner ----------------------------------------------------------
+def zero_step_dp_replicas(W, n, grad_dtype, work_dtype, grads, master, m, v, p16, lr, beta1, beta2, eps, t,
+                          stream=None) -> None:
+    """One DP step over W literal replicas (lists of W device buffers each);
+    no context, the caller keeps t."""
+    _check("zero_step_dp_replicas", lib().zero_step_dp_replicas(
+        W, n, grad_dtype, work_dtype, _ptr_array(grads), _ptr_array(master), _ptr_array(m), _ptr_array(v),
+        _ptr_array(p16), lr, beta1, beta2, eps, t, _stream(stream)))
+
+
+def zero_dp_replicas_mismatches(W, n, master, m, v, p16, mismatches, stream=None) -> None:
+    """Enqueue the bitwise comparison of every replica with replica 0; the
+    count lands in the device int64 ``mismatches``."""
+    _check("zero_dp_replicas_mismatches", lib().zero_dp_replicas_mismatches(
+        W, n, _ptr_array(master), _ptr_array(m), _ptr_array(v), _ptr_array(p16), _ptr(mismatches),
+        _stream(stream)))
+
+
+# ---- convenience owners ---------------------------------------------------------
 
 _DT = {"fp16": ZERO_FP16, "bf16": ZERO_BF16, ZERO_FP16: ZERO_FP16, ZERO_BF16: ZERO_BF16}
 
@@ -388,3 +407,56 @@ class ZeroStep:
             self.close()
         except Exception:
             pass
+
+
+class DpReplicas:
+    """W literal DP replicas allocated with PyTorch on ``device``: per replica
+    an fp32 master, m and v and a 16-bit working copy, n_pad values each.
+
+    ``theta0`` (n fp32 values) is written into every replica's master; m and
+    v start at zero.  Each 16-bit working copy is written by the step (it
+    holds zeros before the first one).  The step and the replica check run
+    in the library.
+    """
+
+    def __init__(self, W, n, grad_dtype="fp16", work_dtype=None, theta0=None, device="cuda", stream=None):
+        import torch
+        self.torch = torch
+        self.W, self.n = int(W), int(n)
+        self.gdt = _DT[grad_dtype]
+        self.wdt = _DT[work_dtype if work_dtype is not None else grad_dtype]
+        self.n_pad = zero_buffer_sizes(ZERO_SCHEME_DP, self.W, [self.n])["n_pad"]
+        self.device = torch.device(device)
+        t16 = {ZERO_FP16: torch.float16, ZERO_BF16: torch.bfloat16}
+        self.grad_torch_dtype, self.work_torch_dtype = t16[self.gdt], t16[self.wdt]
+        need = self.W * self.n_pad * (12 + 2)
+        if self.device.type == "cuda":
+            free, _ = torch.cuda.mem_get_info(self.device)
+            if need > free:
+                raise MemoryError(f"{self.W} replicas of {self.n_pad} parameters need {need} bytes of device "
+                                  f"memory; {free} are free")
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.master = [torch.zeros(self.n_pad, **f32) for _ in range(self.W)]
+        self.m = [torch.zeros(self.n_pad, **f32) for _ in range(self.W)]
+        self.v = [torch.zeros(self.n_pad, **f32) for _ in range(self.W)]
+        self.p16 = [torch.zeros(self.n_pad, dtype=self.work_torch_dtype, device=self.device) for _ in range(self.W)]
+        if theta0 is not None:
+            th = torch.as_tensor(theta0).to(device=self.device, dtype=torch.float32)
+            for r in range(self.W):
+                self.master[r][: self.n].copy_(th)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self._count = torch.zeros(1, dtype=torch.int64, device=self.device)
+
+    def new_grad_buffers(self):
+        return [self.torch.zeros(self.n_pad, dtype=self.grad_torch_dtype, device=self.device) for _ in range(self.W)]
+
+    def step(self, grads, lr, beta1, beta2, eps, t):
+        zero_step_dp_replicas(self.W, self.n, self.gdt, self.wdt, grads, self.master, self.m, self.v, self.p16,
+                              lr, beta1, beta2, eps, t, self.stream)
+
+    def mismatches(self) -> int:
+        """Elements, over replicas 1..W-1, that differ bitwise from replica 0 (waits)."""
+        zero_dp_replicas_mismatches(self.W, self.n, self.master, self.m, self.v, self.p16, self._count,
+                                    self.stream)
+        self.stream.synchronize()
+        return int(self._count.item())

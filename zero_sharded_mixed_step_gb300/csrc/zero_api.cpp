@@ -568,6 +568,14 @@ int run_host_step(zero_ctx* c, const void* const* host_grads, void* host_out, ch
 
 }  // namespace
 
+int zero::check_adam_args(double lr, double beta1, double beta2, double eps, int64_t t) {
+  return check_hyper(lr, beta1, beta2, eps, t);
+}
+
+zero::AdamCoef zero::adam_coef(double lr, double beta1, double beta2, double eps, int64_t t, int W) {
+  return make_coef(lr, beta1, beta2, eps, t, W);
+}
+
 extern "C" {
 
 const char* zero_last_error(void) { return g_last_error.c_str(); }

@@ -92,4 +92,11 @@ int sm_count();
 // Set the calling thread's zero_last_error() message; returns code.
 int record_error(int code, const char* msg);
 
+// Check Adam's hyper-parameters and the step counter t >= 1; on failure
+// records the message and returns ZERO_E_ARG or ZERO_E_STATE.
+int check_adam_args(double lr, double beta1, double beta2, double eps, int64_t t);
+
+// The fp32 coefficients of Adam step t for W ranks, derived in fp64.
+AdamCoef adam_coef(double lr, double beta1, double beta2, double eps, int64_t t, int W);
+
 }  // namespace zero
