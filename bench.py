@@ -13,7 +13,7 @@ that passes through every stage; ``--workload`` selects the GPT-2-small
 
 Prints one JSON line.  ``value`` is whole-job parameters per second with the
 inputs resident in HBM; ``e2e`` is the same metric with the gradients copied
-in from pinned host memory and the 16-bit working copy read back every step;
+in from page-locked host memory and the 16-bit working copy read back every step;
 ``roofline`` is for the fused reduce-scatter + Adam + recast kernel, timed
 per launch with CUDA events on its own stream inside the timed region;
 ``cpu_baseline`` is the CPU oracle timed on a bounded sample on this host.
@@ -63,7 +63,7 @@ def parse_args(argv=None):
     p.add_argument("--units", type=int, default=None,
                    help="ZeRO-3 only: keep the first N units (a smaller copy of the workload with the same "
                         "per-unit launches, for profiling)")
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
@@ -438,20 +438,22 @@ def run_ours(args):
         gather_info = {"launch_ms": gather_ms / gather_n, "achieved_gbs": gb / (gather_ms / gather_n / 1e3) / 1e9,
                        "launches": gather_n, "share_of_bracketed_time": gather_ms / (gather_ms + fused_ms)}
 
-    # ---- end to end: gradients from pinned host memory, working copy read back ------
+    # ---- end to end: gradients from page-locked host memory, working copy read back --
     # through zero_step_host, the C-ABI call that takes host buffers: each step
     # streams the W ranks' gradients over the host link into a two-slot device
     # staging ring and returns the updated 16-bit working copy to host memory,
     # pipelined chunk by chunk (unit by unit for ZeRO-3) on three streams.
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
-        host_grads = []
-        for g in step.grads:                     # straight into pinned memory, no pageable copy
-            h = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+        # host buffers from zero_host_alloc: page-locked on huge pages, where the
+        # link holds its full rate (memory from cudaHostAlloc measured slower)
+        host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in step.grads]
+        host_grads = [b.tensor for b in host_bufs]
+        for h, g in zip(host_grads, step.grads):
             h.copy_(g)
-            host_grads.append(h)
         out_elems = step.n_pad if scheme != 3 else wl.W * step.sizes["shard_store"]
-        host_out = torch.empty(out_elems, dtype=step.work_torch_dtype, pin_memory=True)
+        host_bufs.append(zs.HostBuffer(out_elems, step.work_torch_dtype))
+        host_out = host_bufs[-1].tensor
         need = zs.zero_host_staging_bytes(scheme, wl.W, units, 0)
         staging = torch.empty(need, dtype=torch.uint8, device=dev)
         sh, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -461,7 +463,15 @@ def run_ours(args):
             t += 1
             zs.zero_step_host(step.ctx, scheme, wl.W, wl.n, host_grads, host_out, staging, need, 0, *hp, t, sh, sd)
 
-        host_step()                      # warm the path once, untimed
+        if scheme != 3:
+            back = [(host_out, step.p16)]
+        else:
+            S16 = step.sizes["shard_store"]
+            back = [(host_out[r * S16:(r + 1) * S16], step.shard16[r]) for r in range(wl.W)]
+        link = link_probe(list(zip(step.grads, host_grads)), back, sh)
+        link["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
+        for _ in range(2):               # warm the path, untimed
+            host_step()
         step.sync()
         if world > 1:
             dist.barrier()
@@ -475,9 +485,11 @@ def run_ours(args):
         e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "staging_bytes": need,
-               "path": "zero_step_host: pinned host gradients -> 2-slot device staging ring -> fused step -> "
-                       "16-bit working copy -> pinned host, pipelined over three streams"}
+               "path": "zero_step_host: host gradients (zero_host_alloc) -> 2-slot device staging ring -> "
+                       "fused step -> 16-bit working copy -> host, pipelined over three streams", "link": link}
         del host_grads, host_out, staging
+        for b in host_bufs:
+            b.close()
 
     step.close()
     cpu = None
@@ -498,6 +510,55 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def link_probe(h2d_pairs, d2h_pairs, stream):
+    """The host link's rate right now: the step's own host->device copies
+    and its read-back as plain copies, timed on their own, so that an
+    end-to-end number can be read against the link it ran on (the link is
+    shared with other jobs on the machine and varies between runs).
+    Pairs are (destination, source) tensors."""
+    import torch
+    h2d = sum(src.numel() * src.element_size() for _, src in h2d_pairs)
+    d2h = sum(src.numel() * src.element_size() for _, src in d2h_pairs)
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for dst, src in h2d_pairs:
+            dst.copy_(src, non_blocking=True)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        for dst, src in d2h_pairs:
+            dst.copy_(src, non_blocking=True)
+        stream.synchronize()
+        t2 = time.perf_counter()
+    return {"h2d_gbs": h2d / (t1 - t0) / 1e9, "d2h_gbs": d2h / (t2 - t1) / 1e9, "floor_ms": 1e3 * (t1 - t0),
+            "note": "plain copies of the step's bytes timed just before the end-to-end steps; "
+                    "floor = the step's gradients carried in at that rate"}
+
+
+def huge_page_fraction(bufs) -> float | None:
+    """Share of the host buffers' mapped bytes that the kernel backs with
+    transparent huge pages (from /proc/self/smaps; None where unreadable)."""
+    try:
+        spans = {}
+        cur = None
+        for line in open("/proc/self/smaps"):
+            head = line.split()
+            if head and "-" in head[0] and line[0] in "0123456789abcdef":
+                lo, hi = (int(x, 16) for x in head[0].split("-"))
+                cur = (lo, hi)
+            elif cur and head and head[0] == "AnonHugePages:":
+                spans[cur] = int(head[1]) * 1024
+        want = got = 0
+        for b in bufs:
+            for (lo, hi), huge in spans.items():
+                if lo <= b.ptr < hi:
+                    want += b.nbytes
+                    got += min(huge, b.nbytes)
+        return got / want if want else None
+    except OSError:
+        return None
 
 
 def gpu_uuid(dev):
@@ -565,16 +626,16 @@ def run_replicas(args, wl, dtype, world, rank, dev):
                 "launch_ms": ms_per_step, "algorithmic_bytes_per_launch": step_bytes,
                 "bytes_per_element": per_elem, "frac_of_8tbs_nominal": achieved / 8000.0, "launches_timed": launches}
 
-    # end to end: every step copies the W gradient vectors in from pinned
-    # host memory and reads replica 0's 16-bit working copy back
+    # end to end: every step copies the W gradient vectors in from page-locked
+    # host memory (zero_host_alloc) and reads replica 0's 16-bit working copy back
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
-        host_grads = []
-        for g in grads:
-            h = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+        host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in grads]
+        host_grads = [b.tensor for b in host_bufs]
+        for h, g in zip(host_grads, grads):
             h.copy_(g)
-            host_grads.append(h)
-        host_out = torch.empty(rep.n_pad, dtype=rep.work_torch_dtype, pin_memory=True)
+        host_bufs.append(zs.HostBuffer(rep.n_pad, rep.work_torch_dtype))
+        host_out = host_bufs[-1].tensor
 
         def host_step():
             nonlocal t
@@ -585,7 +646,10 @@ def run_replicas(args, wl, dtype, world, rank, dev):
                 rep.step(grads, *hp, t)
                 host_out.copy_(rep.p16[0], non_blocking=True)
 
-        host_step()
+        link = link_probe(list(zip(grads, host_grads)), [(host_out, rep.p16[0])], su)
+        link["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
+        for _ in range(2):               # warm the path, untimed
+            host_step()
         su.synchronize()
         if world > 1:
             dist.barrier()
@@ -598,9 +662,12 @@ def run_replicas(args, wl, dtype, world, rank, dev):
                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
-               "path": "pinned host gradients -> device gradient buffers (one copy per rank) -> "
-                       "zero_step_dp_replicas -> replica 0's 16-bit working copy -> pinned host, one stream"}
+               "path": "host gradients (zero_host_alloc) -> device gradient buffers (one copy per rank) -> "
+                       "zero_step_dp_replicas -> replica 0's 16-bit working copy -> host, one stream",
+               "link": link}
         del host_grads, host_out
+        for b in host_bufs:
+            b.close()
 
     resident = sum(x.numel() * x.element_size() for x in rep.master + rep.m + rep.v + rep.p16)
     del rep, grads

@@ -65,6 +65,7 @@ extern "C" {
 #define ZERO_E_RANK     -4  /* a simulated rank is marked unavailable            */
 #define ZERO_E_TIMEOUT  -5  /* zero_sync's deadline passed before the work ended */
 #define ZERO_E_STATE    -6  /* call out of order (step counter, unit not live)   */
+#define ZERO_E_NOMEM    -7  /* host memory could not be mapped                   */
 
 /* ---- schemes ("The four schemes": shard_opt / shard_grad / shard_param) - */
 #define ZERO_SCHEME_DP  0   /* nothing sharded, gradients all-reduced           */
@@ -287,6 +288,30 @@ int64_t zero_host_staging_bytes(int scheme, int W, int64_t n_units, const int64_
 int zero_step_host(zero_ctx* ctx, int scheme, int W, int64_t n, const void* const* host_grads, void* host_out,
                    void* staging, int64_t staging_bytes, int64_t chunk_elems, double lr, double beta1,
                    double beta2, double eps, int64_t t, void* stream_h2d, void* stream_d2h);
+
+/*
+ * Host memory for zero_step_host's gradients and results: `bytes` bytes,
+ * page-locked (registered with cudaHostRegister, so copies from and to it
+ * run asynchronously at the link's rate), on a private anonymous mapping
+ * advised for transparent huge pages and populated before it is returned.
+ * The pages do not need to be huge for correctness; they help speed.
+ * Measured on GB300 hosts,
+ * 1 GB copies out of memory pinned with cudaHostAlloc ran from 38 to 212
+ * GB/s, slower in later processes on the same host, while copies out of
+ * this memory held 208-212 GB/s.  The start is aligned to the huge-page
+ * size; the contents are zero.  *out receives the address (NULL on
+ * failure).  The memory is the caller's until zero_host_free.
+ * ZERO_E_ARG for bytes <= 0 or out NULL; ZERO_E_NOMEM if the mapping
+ * fails; ZERO_E_CUDA if the registration fails (e.g. no device).
+ */
+int zero_host_alloc(int64_t bytes, void** out);
+
+/*
+ * Release memory from zero_host_alloc (unregister and unmap).  NULL is
+ * accepted; any other pointer that zero_host_alloc did not return is
+ * ZERO_E_ARG.  No work that uses the memory may still be in flight.
+ */
+int zero_host_free(void* p);
 
 /* ---- ZeRO-3 driven by the caller ---------------------------------------- */
 

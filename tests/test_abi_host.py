@@ -283,3 +283,11 @@ def test_dp_replicas_checks_before_any_launch(zlib):
     assert _err(check, W, n, th, m, v, p, fake(300) + 4) == zs.ZERO_E_ALIGN
     assert _err(check, W, n, th, m, None, p, fake(300)) == zs.ZERO_E_ARG
     assert _err(check, W, n, th, m, v, p[:2] + [p[2] + 1], fake(300)) == zs.ZERO_E_ALIGN
+
+
+def test_host_alloc_checks(zlib):
+    assert _err(zs.zero_host_alloc, 0) == zs.ZERO_E_ARG
+    assert _err(zs.zero_host_alloc, -5) == zs.ZERO_E_ARG
+    assert _err(zs.zero_host_free, 0x1000) == zs.ZERO_E_ARG
+    assert "zero_host_alloc" in zs.zero_last_error()
+    zs.zero_host_free(None)

@@ -11,13 +11,16 @@ import zero_sharded_mixed_step_gb300 as zs
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # scheme, n or units, W, dtype, chunk_elems, pinned, read back
-    (zs.ZERO_SCHEME_Z2, 3_000_005, 8, "bf16", 1_000_000, True, True),
-    (zs.ZERO_SCHEME_Z1, 1_000_003, 3, "fp16", 100_001, True, True),
-    (zs.ZERO_SCHEME_DP, 2_500_000, 16, "bf16", 0, False, True),
-    (zs.ZERO_SCHEME_Z1, 777_777, 8, "bf16", 65_536, True, False),
-    (zs.ZERO_SCHEME_Z3, [1_000_003, 17, 0, 250_000, 7], 5, "bf16", 0, True, True),
-    (zs.ZERO_SCHEME_Z3, [262_144, 262_144, 262_144], 8, "fp16", 0, False, True),
+    # scheme, n or units, W, dtype, chunk_elems, host memory, read back;
+    # host memory: "pin" torch pinned, "page" pageable, "huge" zero_host_alloc
+    (zs.ZERO_SCHEME_Z2, 3_000_005, 8, "bf16", 1_000_000, "pin", True),
+    (zs.ZERO_SCHEME_Z1, 1_000_003, 3, "fp16", 100_001, "pin", True),
+    (zs.ZERO_SCHEME_DP, 2_500_000, 16, "bf16", 0, "page", True),
+    (zs.ZERO_SCHEME_Z1, 777_777, 8, "bf16", 65_536, "pin", False),
+    (zs.ZERO_SCHEME_Z3, [1_000_003, 17, 0, 250_000, 7], 5, "bf16", 0, "pin", True),
+    (zs.ZERO_SCHEME_Z3, [262_144, 262_144, 262_144], 8, "fp16", 0, "page", True),
+    (zs.ZERO_SCHEME_Z2, 2_000_003, 8, "bf16", 500_000, "huge", True),
+    (zs.ZERO_SCHEME_Z3, [500_000, 3, 700_001], 8, "bf16", 0, "huge", True),
 ]
 
 
@@ -28,9 +31,20 @@ def _built():
     assert torch.cuda.is_available()
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"s{c[0]}_W{c[2]}_{c[3]}_chunk{c[4]}_pin{int(c[5])}_out{int(c[6])}")
+def _host_copy(g, mem, keep):
+    if mem == "pin":
+        return g.cpu().pin_memory()
+    if mem == "page":
+        return g.cpu()
+    buf = zs.HostBuffer(g.numel(), g.dtype)
+    keep.append(buf)
+    buf.tensor.copy_(g)
+    return buf.tensor
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"s{c[0]}_W{c[2]}_{c[3]}_chunk{c[4]}_{c[5]}_out{int(c[6])}")
 def test_host_step_equals_device_step(case):
-    scheme, size, W, dtype, chunk, pinned, read_back = case
+    scheme, size, W, dtype, chunk, mem, read_back = case
     units = size if isinstance(size, list) else [size]
     n = sum(units)
     wl = wk.scaled(wk.GPT2_SMALL, unit_sizes=units if scheme == zs.ZERO_SCHEME_Z3 else None, n=n, W=W, steps=3,
@@ -41,7 +55,14 @@ def test_host_step_equals_device_step(case):
     need = zs.zero_host_staging_bytes(scheme, W, units, chunk)
     staging = torch.empty(need, dtype=torch.uint8, device="cuda")
     out_elems = b.n_pad if scheme != zs.ZERO_SCHEME_Z3 else W * b.sizes["shard_store"]
-    host_out = torch.zeros(out_elems, dtype=b.work_torch_dtype, pin_memory=True) if read_back else None
+    keep = []
+    if not read_back:
+        host_out = None
+    elif mem == "huge":
+        keep.append(zs.HostBuffer(out_elems, b.work_torch_dtype))
+        host_out = keep[-1].tensor
+    else:
+        host_out = torch.zeros(out_elems, dtype=b.work_torch_dtype, pin_memory=True)
     sh, sd = torch.cuda.Stream(), torch.cuda.Stream()
     src = wk.GradSource(wl, dtype, "cuda")
     hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
@@ -51,7 +72,7 @@ def test_host_step_equals_device_step(case):
             g = torch.zeros(a.n_pad, dtype=a.grad_torch_dtype, device="cuda")
             a.place_(g, d)
             dev_grads.append(g)
-        host = [g.cpu().pin_memory() if pinned else g.cpu() for g in dev_grads]
+        host = [_host_copy(g, mem, keep) for g in dev_grads]
         torch.cuda.synchronize()
         a.step(dev_grads, *hp, t)
         zs.zero_step_host(b.ctx, scheme, W, n, host, host_out, staging, need, chunk, *hp, t, sh, sd)
@@ -70,3 +91,29 @@ def test_host_step_equals_device_step(case):
     assert b.stat(zs.ZERO_STAT_LIVE_ELEMS) == 0
     a.close()
     b.close()
+    torch.cuda.synchronize()
+    for buf in keep:
+        buf.close()
+
+
+def test_host_alloc_is_page_locked_aligned_and_zeroed():
+    """zero_host_alloc: the memory starts on a huge-page boundary, reads as
+    zeros, counts as page-locked for CUDA copies, and is returned by
+    zero_host_free (twice is an error: the address is no longer known)."""
+    try:
+        huge = int(open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size").read())
+    except OSError:
+        huge = 2 << 20
+    buf = zs.HostBuffer((3 << 20) + 5, torch.float16)
+    assert buf.ptr % huge == 0
+    assert buf.tensor.is_pinned()
+    assert int(buf.tensor.view(torch.int16).abs().max()) == 0
+    d = torch.arange(buf.tensor.numel(), device="cuda").to(torch.float16)
+    buf.tensor.copy_(d, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(buf.tensor, d.cpu())
+    ptr = buf.ptr
+    buf.close()
+    with pytest.raises(zs.ZeroError) as e:
+        zs.zero_host_free(ptr)
+    assert e.value.code == zs.ZERO_E_ARG

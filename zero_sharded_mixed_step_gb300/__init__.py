@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libzero_gb300.so")
 
 # constants of include/zero_step.h
 ZERO_OK, ZERO_E_ARG, ZERO_E_ALIGN, ZERO_E_CUDA, ZERO_E_RANK, ZERO_E_TIMEOUT, ZERO_E_STATE = 0, -1, -2, -3, -4, -5, -6
+ZERO_E_NOMEM = -7
 ZERO_SCHEME_DP, ZERO_SCHEME_Z1, ZERO_SCHEME_Z2, ZERO_SCHEME_Z3 = 0, 1, 2, 3
 ZERO_FP16, ZERO_BF16 = 0, 1
 ZERO_RESIDENT, ZERO_PEAK = 0, 1
@@ -34,7 +35,8 @@ ZERO_KERNEL_FUSED, ZERO_KERNEL_GATHER, ZERO_KERNEL_CAST = 0, 1, 2
 ZERO_DEBUG_POISON_RELEASED = 1
 
 ERROR_NAMES = {ZERO_E_ARG: "ZERO_E_ARG", ZERO_E_ALIGN: "ZERO_E_ALIGN", ZERO_E_CUDA: "ZERO_E_CUDA",
-               ZERO_E_RANK: "ZERO_E_RANK", ZERO_E_TIMEOUT: "ZERO_E_TIMEOUT", ZERO_E_STATE: "ZERO_E_STATE"}
+               ZERO_E_RANK: "ZERO_E_RANK", ZERO_E_TIMEOUT: "ZERO_E_TIMEOUT", ZERO_E_STATE: "ZERO_E_STATE",
+               ZERO_E_NOMEM: "ZERO_E_NOMEM"}
 
 # every symbol the header declares, with (restype, argtypes)
 _P, _I, _L, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
@@ -54,6 +56,8 @@ SIGNATURES = {
     "zero_step_bucket": (_I, [_P, _L, _L, _PP, _D, _D, _D, _D, _L, _P]),
     "zero_host_staging_bytes": (_L, [_I, _I, _L, _LP, _L]),
     "zero_step_host": (_I, [_P, _I, _I, _L, _PP, _P, _P, _L, _L, _D, _D, _D, _D, _L, _P, _P]),
+    "zero_host_alloc": (_I, [_L, ctypes.POINTER(_P)]),
+    "zero_host_free": (_I, [_P]),
     "zero_gather_unit": (_I, [_P, _L, _P, _P]),
     "zero_release_unit": (_I, [_P, _L]),
     "zero_update_unit": (_I, [_P, _L, _PP, _D, _D, _D, _D, _L, _P]),
@@ -201,6 +205,43 @@ def zero_step_host(ctx, scheme, W, n, host_grads, host_out, staging, staging_byt
     _check("zero_step_host", lib().zero_step_host(
         ctx, scheme, W, n, _ptr_array(host_grads), _ptr(host_out), _ptr(staging), staging_bytes, chunk_elems,
         lr, beta1, beta2, eps, t, _stream(stream_h2d), _stream(stream_d2h)))
+
+
+def zero_host_alloc(nbytes: int) -> int:
+    """Page-locked host memory on huge pages for the host-fed step; returns its address."""
+    p = ctypes.c_void_p()
+    _check("zero_host_alloc", lib().zero_host_alloc(int(nbytes), ctypes.byref(p)))
+    return p.value
+
+
+def zero_host_free(ptr) -> None:
+    _check("zero_host_free", lib().zero_host_free(ptr))
+
+
+class HostBuffer:
+    """A zero_host_alloc block seen as a CPU tensor of ``numel`` values of
+    ``dtype`` (the tensor shares the memory; keep this object alive while it
+    or any copy in flight uses it, then ``close()``)."""
+
+    def __init__(self, numel: int, dtype):
+        import torch
+        itemsize = torch.empty(0, dtype=dtype).element_size()
+        self.nbytes = max(1, int(numel) * itemsize)
+        self.ptr = zero_host_alloc(self.nbytes)
+        raw = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        self.tensor = torch.frombuffer(raw, dtype=torch.uint8)[: int(numel) * itemsize].view(dtype)
+
+    def close(self):
+        if self.ptr:
+            self.tensor = None
+            zero_host_free(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def zero_set_unit_hook(ctx, fn, user=None):

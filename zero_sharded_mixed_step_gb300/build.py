@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libzero_gb300.so")
-SOURCES = ["zero_api.cpp", "fused_step.cu", "copy_cast.cu", "zero3_static.cu", "dp_replicas.cu"]
+SOURCES = ["zero_api.cpp", "fused_step.cu", "copy_cast.cu", "zero3_static.cu", "dp_replicas.cu",
+           "host_memory.cpp"]
 HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "step_math.cuh"),
            os.path.join(INCLUDE, "zero_step.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
