@@ -55,7 +55,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="zero3_24x50m_w8",
                    choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1",
-                            "gpt2_small_124m_w8_dp_replicas"])
+                            "gpt2_small_124m_w8_dp_replicas", "gpt2_small_124m_w8_zero2_offload"])
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None)
     p.add_argument("--params", type=int, default=None,
                    help="flat workloads only: a smaller copy with this many parameters (same W, dtype, "
@@ -303,7 +303,8 @@ def config_of(wl, dtype, gpus):
     n_pad, per_launch, units = layout_sizes(wl)
     fused, gathers = algorithmic_bytes(wl)
     names = {0: "data parallel", 1: "ZeRO-1", 2: "ZeRO-2", 3: "ZeRO-3"}
-    scheme = names[scheme_of(wl)] + (f", {wl.W} replicas kept literally" if wl.dp_replicas else "")
+    scheme = names[scheme_of(wl)] + (f", {wl.W} replicas kept literally" if wl.dp_replicas else "") + \
+        (", optimizer state and update on the host CPU" if wl.offload else "")
     return {"workload": wl.name, "scheme": scheme, "W": wl.W, "params": wl.n, "padded": n_pad,
             "units": len(units), "grad_dtype": dtype, "work_dtype": dtype, "master_dtype": "f32",
             "algorithmic_bytes_per_step": fused + gathers,
@@ -357,6 +358,8 @@ def run_ours(args):
     dtype = args.dtype or wl.dtypes[0]
     if wl.dp_replicas:
         return run_replicas(args, wl, dtype, world, rank, dev)
+    if wl.offload:
+        return run_offload(args, wl, dtype, world, rank, dev)
     scheme = scheme_of(wl)
     n_pad, per_launch, units = layout_sizes(wl)
     su = torch.cuda.Stream(dev)
@@ -682,6 +685,145 @@ def run_replicas(args, wl, dtype, world, rank, dev):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
             "step_hbm_gbs": achieved, "step_frac_of_peak": achieved / peak,
+            "roofline": roofline, "gather": None, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def host_copy_gbs(threads: int, nbytes: int = 1 << 31) -> float:
+    """Measured host memory bandwidth: a multi-threaded copy of nbytes
+    (read + write bytes per second), the denominator of the host update."""
+    import torch
+    old = torch.get_num_threads()
+    torch.set_num_threads(threads)
+    try:
+        a = torch.ones(nbytes // 4, dtype=torch.float32)
+        b = torch.empty_like(a)
+        b.copy_(a)
+        best = 0.0
+        for _ in range(5):
+            t0 = time.perf_counter()
+            b.copy_(a)
+            best = max(best, 2 * nbytes / (time.perf_counter() - t0) / 1e9)
+        return best
+    finally:
+        torch.set_num_threads(old)
+
+
+def run_offload(args, wl, dtype, world, rank, dev):
+    """ZeRO-2 with the optimizer on the host (zero_offload_step): the GPU forms
+    the mean gradient, host threads run Adam on host-resident fp32 state, the
+    16-bit copy streams back.  Same line as the other workloads; the roofline
+    is that of the host update, which bounds the step."""
+    import torch
+    import torch.distributed as dist
+    import zero_sharded_mixed_step_gb300 as zs
+    import workloads as wk
+
+    su = torch.cuda.Stream(dev)
+    with torch.cuda.stream(su):
+        theta0 = wk.draw_theta0(wl, dev)
+        off = zs.ZeroOffload(wl.W, wl.n, dtype, theta0=theta0.cpu(), device=dev, stream=su)
+        del theta0
+        grads = off.new_grad_buffers()
+        for g, d in zip(grads, wk.GradSource(wl, dtype, dev).step(1)):
+            g[: wl.n].copy_(d)
+            del d
+    torch.cuda.synchronize()
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        off.step(grads, *hp, t)
+    torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    st0 = off.stats()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid(dev)) as clocks:
+        e0.record(su)
+        for _ in range(args.steps):
+            t += 1
+            off.step(grads, *hp, t)
+        e1.record(su)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st1 = off.stats()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms_per_step = ms / args.steps
+    value = whole_job_value(world, wl.n, args.steps, ms)
+    host_s = (st1["host_seconds"] - st0["host_seconds"]) / args.steps
+    host_bytes = 30 * off.n_pad          # read mean 4 + master, m, v 12; write 12 + 16-bit 2
+    achieved = host_bytes / host_s / 1e9
+    peak = host_copy_gbs(st1["threads"])
+    roofline = {"bound": "host_dram", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "host Adam (zero_offload_step's host update)",
+                "peak_source": f"host copy measured in this run ({st1['threads']} threads, read + write)",
+                "host_ms_per_step": 1e3 * host_s, "algorithmic_bytes_per_step": host_bytes, "bytes_per_element": 30,
+                "threads": st1["threads"]}
+    launches = st1["launches"] - st0["launches"]
+    link = {"d2h_bytes_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.steps,
+            "h2d_bytes_per_step": (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.steps}
+
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in grads]
+        host_grads = [b.tensor for b in host_bufs]
+        for h, g in zip(host_grads, grads):
+            h.copy_(g)
+        host_bufs.append(zs.HostBuffer(off.n_pad, off.work_torch_dtype))
+        host_out = host_bufs[-1].tensor
+
+        def host_step():
+            nonlocal t
+            t += 1
+            with torch.cuda.stream(su):
+                for g, h in zip(grads, host_grads):
+                    g.copy_(h, non_blocking=True)
+                off.step(grads, *hp, t)
+                host_out.copy_(off.p16, non_blocking=True)
+
+        probe = link_probe(list(zip(grads, host_grads)), [(host_out, off.p16)], su)
+        probe["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
+        for _ in range(2):
+            host_step()
+        su.synchronize()
+        h0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            host_step()
+        su.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - h0)
+        e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
+               "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
+               "path": "host gradients (zero_host_alloc) -> device gradient buffers -> zero_offload_step "
+                       "(device mean, host Adam, 16-bit copy back) -> 16-bit working copy -> host",
+               "link": probe}
+        del host_grads, host_out
+        for b in host_bufs:
+            b.close()
+
+    off.close()
+    del grads
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, dtype, args.cpu_seconds)
+    if rank == 0:
+        config = config_of(wl, dtype, world)
+        config["algorithmic_bytes_per_step"] = (2 * wl.W + 4) * off.n_pad + host_bytes
+        config["offload_link_bytes_per_step"] = link
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
             "roofline": roofline, "gather": None, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks.summary(),
         }

@@ -510,6 +510,84 @@ int zero_dp_replicas_mismatches(int W, int64_t n, const float* const* master, co
                                 const float* const* v, const void* const* p16, int64_t* mismatches,
                                 void* stream);
 
+/* ---- the optimizer offloaded to the host ------------------------------------ */
+
+/*
+ * ZeRO-2 with the optimizer state and its update on the host CPU ("ZeRO and
+ * FSDP", ZeRO-3 and FSDP, and "Sharding the States": offloading puts the
+ * optimizer states in CPU memory, trading link bandwidth for device memory;
+ * "ZeRO, annotated" section 11: ZeRO-Offload moves the optimizer's
+ * computation to the CPU too).  The device keeps the W ranks' 16-bit
+ * gradients and the 16-bit working copy; the fp32 master, m and v live in
+ * host memory.  Per step, chunk by chunk: the GPU forms the rank-ordered fp32
+ * mean of the W gradients (the reduce-scatter), copy engines carry it to the
+ * host (4 bytes per element), a pool of host threads runs Adam and the
+ * round-to-nearest-even recast, and copy engines carry the 16-bit values back
+ * into the device working copy (2 bytes per element).  The host arithmetic
+ * repeats the device kernel's operations one for one in IEEE single
+ * precision, so the result is bit-identical to zero_step.  Only this entry
+ * point and zero_adam_host compute on the host; no GPU entry point falls back
+ * to them.
+ */
+typedef struct zero_offload zero_offload;
+
+/* Device staging the offloaded step needs: two chunks of fp32 means
+ * (chunk_elems <= 0: the default of 4,194,304 elements; rounded up to a
+ * multiple of 8). */
+int64_t zero_offload_staging_bytes(int64_t chunk_elems);
+
+/*
+ * Create an offloaded-step context.  Layout as for ZERO_SCHEME_Z2 (one unit,
+ * n_pad = ceil(n / W) * W values per vector, rank r owning [r S, (r + 1) S)).
+ *   host_master, host_m, host_v  host memory, n_pad floats each; master holds
+ *                theta0 (padding zero), m and v zeros.  Read and written by the
+ *                host threads only.
+ *   host_grad    host memory for n_pad fp32 means; host_p16 host memory for
+ *                n_pad 16-bit values.  Both should be page-locked (e.g. from
+ *                zero_host_alloc) so that their copies run asynchronously.
+ *   p16          device, n_pad 16-bit values (work_dtype), 16-byte aligned:
+ *                the working copy, overwritten by each step.
+ *   staging      device, >= zero_offload_staging_bytes(chunk_elems) bytes,
+ *                256-byte aligned.
+ *   threads      host threads for Adam (<= 0: all hardware threads).
+ *   stream       cudaStream_t the GPU work is enqueued on (NULL: legacy default).
+ * All buffers stay the caller's.  The context owns two copy streams, its
+ * events and its threads.
+ */
+int zero_offload_init(zero_offload** out, int W, int64_t n, int grad_dtype, int work_dtype, float* host_master,
+                      float* host_m, float* host_v, float* host_grad, void* host_p16, void* p16, void* staging,
+                      int64_t staging_bytes, int64_t chunk_elems, int threads, void* stream);
+
+/*
+ * One offloaded step.  grads: host array of W device pointers (n_pad values
+ * of grad_dtype each, 16-byte aligned).  t must follow the context's last
+ * step counter (ZERO_E_STATE otherwise).  The call returns when the host
+ * update is done; the copies of the new working copy may still be in
+ * flight, and work enqueued later on `stream` runs after them.  A chunk whose
+ * mean has not reached host memory within 60 s gives ZERO_E_TIMEOUT.
+ */
+int zero_offload_step(zero_offload* ctx, const void* const* grads, double lr, double beta1, double beta2,
+                      double eps, int64_t t);
+
+/* Cumulative figures of a context (any pointer may be NULL): the last step
+ * counter, seconds the host spent in Adam, bytes copied device->host and
+ * host->device, kernels launched, host threads. */
+int zero_offload_stats(const zero_offload* ctx, int64_t* t, double* host_seconds, int64_t* d2h_bytes,
+                       int64_t* h2d_bytes, int64_t* launches, int* threads);
+
+/* Destroy a context (waits for its work). NULL is accepted. */
+int zero_offload_destroy(zero_offload* ctx);
+
+/*
+ * The offloaded step's host update alone, on host memory: Adam step t for
+ * W ranks (W fixes only the mean's 1/W coefficient, unused here) on n
+ * elements with mean gradient `grad`, updating master, m and v in place and
+ * writing the round-to-nearest-even 16-bit copy (work_dtype) to out16.
+ * threads as above.  Needs no GPU.
+ */
+int zero_adam_host(int64_t n, const float* grad, float* master, float* m, float* v, void* out16, int work_dtype,
+                   double lr, double beta1, double beta2, double eps, int64_t t, int W, int threads);
+
 /* Message for the calling thread's last error ("" if none). */
 const char* zero_last_error(void);
 

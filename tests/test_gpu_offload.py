@@ -1,0 +1,107 @@
+"""ZeRO-2 with the optimizer offloaded to the host (zero_offload_*):
+bitwise against the device step zero_step on the same gradients, and
+against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wk
+import zero_sharded_mixed_step_gb300 as zs
+from oracle import zero_oracle as z
+from tests.gpu_harness import assert_16bit_band, assert_f32_close, bits_of, sample_real_indices
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # n, W, grad dtype, working dtype, chunk_elems (0: default; others rounded up to 8)
+    (1001, 3, wk.FP16, wk.FP16, 64),
+    (3_000_005, 8, wk.BF16, wk.BF16, 1 << 20),
+    (2_000_000, 16, wk.FP16, wk.BF16, 0),
+    (7, 1, wk.BF16, wk.FP16, 8),
+    (250_001, 5, wk.BF16, wk.BF16, 100),
+]
+
+
+def _equal(a, b):
+    return torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a.view(torch.int16),
+                       b.view(torch.int32) if b.dtype == torch.float32 else b.view(torch.int16))
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"n{c[0]}_W{c[1]}_{c[2]}_{c[3]}_chunk{c[4]}")
+def test_offloaded_step_equals_device_step(case):
+    n, W, gdt, wdt, chunk = case
+    wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=3, name="offload")
+    theta0 = wk.draw_theta0(wl, "cuda")
+    dev = zs.ZeroStep(zs.ZERO_SCHEME_Z2, W, [n], gdt, wdt, theta0=theta0)
+    off = zs.ZeroOffload(W, n, gdt, wdt, theta0=theta0.cpu(), chunk_elems=chunk, threads=4)
+    src = wk.GradSource(wl, gdt, "cuda")
+    grads = dev.new_grad_buffers()
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    for t in range(1, wl.steps + 1):
+        for g, d in zip(grads, src.step(t)):
+            g[:n].copy_(d)
+        dev.step(grads, *hp, t)
+        off.step(grads, *hp, t)
+        torch.cuda.synchronize()
+        for mine, theirs in ((off.master, dev.master), (off.m, dev.m), (off.v, dev.v)):
+            assert _equal(mine, theirs.cpu()), t
+        assert _equal(off.p16, dev.p16), t
+        assert bool((off.master[n:] == 0).all())
+    st = off.stats()
+    assert st["t"] == wl.steps
+    assert st["d2h_bytes"] == 4 * off.n_pad * wl.steps
+    assert st["h2d_bytes"] == 2 * off.n_pad * wl.steps
+    with pytest.raises(zs.ZeroError) as e:
+        off.step(grads, *hp, wl.steps + 2)
+    assert e.value.code == zs.ZERO_E_STATE
+    off.close()
+    dev.close()
+
+
+def test_tiny_offloaded_step_against_the_oracle():
+    wl = wk.TINY
+    theta0 = wk.draw_theta0(wl, "cuda")
+    off = zs.ZeroOffload(wl.W, wl.n, wk.FP16, theta0=theta0.cpu(), threads=2)
+    orc = z.make_scheme(z.ZERO2, wl.W, theta0.cpu().numpy(), wk.FP16)
+    src = wk.GradSource(wl, wk.FP16, "cuda")
+    grads = off.new_grad_buffers()
+    for t in range(1, wl.steps + 1):
+        for g, d in zip(grads, src.step(t)):
+            g[:wl.n].copy_(d)
+        off.step(grads, wl.lr, wl.beta1, wl.beta2, wl.eps, t)
+        orc.step([z.place(wk.to_numpy16(g[:wl.n]), orc.layout) for g in grads], wl.lr, wl.beta1, wl.beta2,
+                 wl.eps)
+        torch.cuda.synchronize()
+        assert_f32_close(off.master.numpy(), orc.full_master(), f"t={t} master")
+        assert_f32_close(off.m.numpy(), orc.full_m(), f"t={t} m")
+        assert_f32_close(off.v.numpy(), orc.full_v(), f"t={t} v")
+        assert_16bit_band(bits_of(off.p16), orc.full_master(), wk.FP16, f"t={t} working copy")
+    off.close()
+
+
+def test_gpt2_small_sized_offloaded_step():
+    """124,439,808 parameters on 8 ranks, bf16, two steps: bitwise equal to
+    ZeRO-2 on the device, and a sample against the oracle."""
+    wl = wk.scaled(wk.GPT2_SMALL, steps=2)
+    theta0 = wk.draw_theta0(wl, "cuda")
+    dev = zs.ZeroStep(zs.ZERO_SCHEME_Z2, wl.W, [wl.n], wk.BF16, theta0=theta0)
+    off = zs.ZeroOffload(wl.W, wl.n, wk.BF16, theta0=theta0.cpu())
+    idx = sample_real_indices(wl.n, wl.W, [wl.n], k=4096)
+    orc = z.SingleReplica(theta0.cpu().numpy()[idx], wk.BF16)
+    del theta0
+    src = wk.GradSource(wl, wk.BF16, "cuda")
+    grads = dev.new_grad_buffers()
+    tidx = torch.from_numpy(idx).cuda()
+    for t in range(1, wl.steps + 1):
+        for g, d in zip(grads, src.step(t)):
+            g[:wl.n].copy_(d)
+        dev.step(grads, wl.lr, wl.beta1, wl.beta2, wl.eps, t)
+        off.step(grads, wl.lr, wl.beta1, wl.beta2, wl.eps, t)
+        orc.step([wk.to_numpy16(g[tidx]) for g in grads], wl.lr, wl.beta1, wl.beta2, wl.eps)
+        torch.cuda.synchronize()
+        assert _equal(off.master, dev.master.cpu())
+        assert _equal(off.p16, dev.p16)
+        assert_f32_close(off.master.numpy()[idx], orc.master, f"t={t} master sample")
+    off.close()
+    dev.close()

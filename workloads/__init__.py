@@ -1,7 +1,7 @@
 """Seeded synthetic workloads for the ZeRO step: sizes, hyper-parameters and
 random draws.
 
-This module holds no arithmetic of the method.  It describes the six
+This module holds no arithmetic of the method.  It describes the seven
 workloads (sizes, rank counts, schemes, Adam hyper-parameters, step counts,
 value distributions and seeds) and draws their random inputs with
 ``torch.Generator``: the initial fp32 master and each rank's 16-bit
@@ -63,6 +63,8 @@ class Workload:
     description: str = ""
     # data parallelism with its W replicas kept literally (scheme DP only)
     dp_replicas: bool = False
+    # ZeRO-2 with the optimizer state and update on the host CPU
+    offload: bool = False
 
     def units(self):
         return list(self.unit_sizes) if self.unit_sizes else [self.n]
@@ -114,7 +116,16 @@ GPT2_SMALL_DP_REPLICAS = Workload(
     description="the GPT-2-small vector under plain data parallelism, its 8 replicas kept literally",
 )
 
-WORKLOADS = {w.name: w for w in (TINY, FLAT_1M, GPT2_SMALL, GPT2_XL, LAYER_UNITS, GPT2_SMALL_DP_REPLICAS)}
+GPT2_SMALL_OFFLOAD = Workload(
+    name="gpt2_small_124m_w8_zero2_offload", n=124_439_808, W=8, schemes=(ZERO2,), dtypes=(BF16, FP16),
+    lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, steps=20,
+    theta_sigma=0.02, grad_sigma=1e-3, seed_rule="step_rank",
+    outlier_frac=1e-3, outlier_scale=50.0, offload=True,
+    description="the GPT-2-small vector under ZeRO-2 with the optimizer state and update on the host",
+)
+
+WORKLOADS = {w.name: w for w in (TINY, FLAT_1M, GPT2_SMALL, GPT2_XL, LAYER_UNITS, GPT2_SMALL_DP_REPLICAS,
+                                 GPT2_SMALL_OFFLOAD)}
 
 
 def scaled(wl: Workload, n: int | None = None, W: int | None = None, steps: int | None = None,

@@ -56,6 +56,13 @@ SIGNATURES = {
     "zero_step_bucket": (_I, [_P, _L, _L, _PP, _D, _D, _D, _D, _L, _P]),
     "zero_host_staging_bytes": (_L, [_I, _I, _L, _LP, _L]),
     "zero_step_host": (_I, [_P, _I, _I, _L, _PP, _P, _P, _L, _L, _D, _D, _D, _D, _L, _P, _P]),
+    "zero_offload_staging_bytes": (_L, [_L]),
+    "zero_offload_init": (_I, [ctypes.POINTER(_P), _I, _L, _I, _I, _P, _P, _P, _P, _P, _P, _P, _L, _L, _I, _P]),
+    "zero_offload_step": (_I, [_P, _PP, _D, _D, _D, _D, _L]),
+    "zero_offload_stats": (_I, [_P, _LP, ctypes.POINTER(ctypes.c_double), _LP, _LP, _LP,
+                                ctypes.POINTER(ctypes.c_int)]),
+    "zero_offload_destroy": (_I, [_P]),
+    "zero_adam_host": (_I, [_L, _P, _P, _P, _P, _P, _I, _D, _D, _D, _D, _L, _I, _I]),
     "zero_host_alloc": (_I, [_L, ctypes.POINTER(_P)]),
     "zero_host_free": (_I, [_P]),
     "zero_gather_unit": (_I, [_P, _L, _P, _P]),
@@ -216,6 +223,44 @@ def zero_host_alloc(nbytes: int) -> int:
 
 def zero_host_free(ptr) -> None:
     _check("zero_host_free", lib().zero_host_free(ptr))
+
+
+def zero_offload_staging_bytes(chunk_elems: int = 0) -> int:
+    return _check("zero_offload_staging_bytes", lib().zero_offload_staging_bytes(chunk_elems))
+
+
+def zero_offload_init(W, n, grad_dtype, work_dtype, host_master, host_m, host_v, host_grad, host_p16, p16,
+                      staging, staging_bytes, chunk_elems=0, threads=0, stream=None):
+    ctx = ctypes.c_void_p()
+    _check("zero_offload_init", lib().zero_offload_init(
+        ctypes.byref(ctx), W, n, grad_dtype, work_dtype, _ptr(host_master), _ptr(host_m), _ptr(host_v),
+        _ptr(host_grad), _ptr(host_p16), _ptr(p16), _ptr(staging), staging_bytes, chunk_elems, threads,
+        _stream(stream)))
+    return ctx
+
+
+def zero_offload_step(ctx, grads, lr, beta1, beta2, eps, t) -> None:
+    _check("zero_offload_step", lib().zero_offload_step(ctx, _ptr_array(grads), lr, beta1, beta2, eps, t))
+
+
+def zero_offload_stats(ctx) -> dict:
+    t, d2h, h2d, launches = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    secs, threads = ctypes.c_double(), ctypes.c_int()
+    _check("zero_offload_stats", lib().zero_offload_stats(ctx, ctypes.byref(t), ctypes.byref(secs),
+                                                          ctypes.byref(d2h), ctypes.byref(h2d),
+                                                          ctypes.byref(launches), ctypes.byref(threads)))
+    return {"t": t.value, "host_seconds": secs.value, "d2h_bytes": d2h.value, "h2d_bytes": h2d.value,
+            "launches": launches.value, "threads": threads.value}
+
+
+def zero_offload_destroy(ctx) -> None:
+    _check("zero_offload_destroy", lib().zero_offload_destroy(ctx))
+
+
+def zero_adam_host(n, grad, master, m, v, out16, work_dtype, lr, beta1, beta2, eps, t, W=1, threads=0) -> None:
+    """The offloaded step's host update on host tensors (no GPU needed)."""
+    _check("zero_adam_host", lib().zero_adam_host(n, _ptr(grad), _ptr(master), _ptr(m), _ptr(v), _ptr(out16),
+                                                  work_dtype, lr, beta1, beta2, eps, t, W, threads))
 
 
 class HostBuffer:
@@ -501,3 +546,59 @@ class DpReplicas:
                                     self.stream)
         self.stream.synchronize()
         return int(self._count.item())
+
+
+class ZeroOffload:
+    """ZeRO-2 with the optimizer on the host: fp32 master, m and v in host
+    memory (the 16-bit working copy and the gradients on ``device``), the
+    fp32 means and 16-bit results crossing the link through page-locked
+    buffers from ``zero_host_alloc``.  ``theta0`` (n values) seeds the
+    master; the device working copy is written by each step."""
+
+    def __init__(self, W, n, grad_dtype="fp16", work_dtype=None, theta0=None, device="cuda", stream=None,
+                 chunk_elems=0, threads=0):
+        import torch
+        self.torch = torch
+        self.W, self.n = int(W), int(n)
+        self.gdt = _DT[grad_dtype]
+        self.wdt = _DT[work_dtype if work_dtype is not None else grad_dtype]
+        self.n_pad = zero_buffer_sizes(ZERO_SCHEME_Z2, self.W, [self.n])["n_pad"]
+        self.device = torch.device(device)
+        t16 = {ZERO_FP16: torch.float16, ZERO_BF16: torch.bfloat16}
+        self.grad_torch_dtype, self.work_torch_dtype = t16[self.gdt], t16[self.wdt]
+        self._bufs = [HostBuffer(self.n_pad, torch.float32) for _ in range(4)]
+        self.master, self.m, self.v, self.host_grad = (b.tensor for b in self._bufs)
+        self._bufs.append(HostBuffer(self.n_pad, self.work_torch_dtype))
+        self.host_p16 = self._bufs[-1].tensor
+        if theta0 is not None:
+            self.master[: self.n].copy_(torch.as_tensor(theta0, dtype=torch.float32).cpu())
+        self.p16 = torch.zeros(self.n_pad, dtype=self.work_torch_dtype, device=self.device)
+        self.staging_bytes = zero_offload_staging_bytes(chunk_elems)
+        self.staging = torch.empty(self.staging_bytes, dtype=torch.uint8, device=self.device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.ctx = zero_offload_init(self.W, self.n, self.gdt, self.wdt, self.master, self.m, self.v,
+                                     self.host_grad, self.host_p16, self.p16, self.staging, self.staging_bytes,
+                                     chunk_elems, threads, self.stream)
+
+    def new_grad_buffers(self):
+        return [self.torch.zeros(self.n_pad, dtype=self.grad_torch_dtype, device=self.device) for _ in range(self.W)]
+
+    def step(self, grads, lr, beta1, beta2, eps, t):
+        zero_offload_step(self.ctx, grads, lr, beta1, beta2, eps, t)
+
+    def stats(self):
+        return zero_offload_stats(self.ctx)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            zero_offload_destroy(self.ctx)
+            self.ctx = None
+        for b in getattr(self, "_bufs", []):
+            b.close()
+        self._bufs = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -20,7 +20,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libzero_gb300.so")
 SOURCES = ["zero_api.cpp", "fused_step.cu", "copy_cast.cu", "zero3_static.cu", "dp_replicas.cu",
-           "host_memory.cpp"]
+           "host_memory.cpp", "offload_mean.cu", "offload.cpp"]
+# Host arithmetic must match the device kernel's operation for operation: no
+# contraction of a product and a sum into one fused operation by the compiler
+# (the code writes every fused multiply-add it wants), and no errno from sqrt,
+# which would keep the loop from being vectorised.
+EXTRA_FLAGS = {"offload.cpp": ["-Xcompiler", "-ffp-contract=off", "-Xcompiler", "-fno-math-errno"]}
 HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "step_math.cuh"),
            os.path.join(INCLUDE, "zero_step.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -64,7 +69,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         if force or ptxas_verbose or _stale(obj, [path] + HEADERS):
-            jobs.append([nvcc()] + _flags(ptxas_verbose) + ["-c", path, "-o", obj])
+            jobs.append([nvcc()] + _flags(ptxas_verbose) + EXTRA_FLAGS.get(src, []) + ["-c", path, "-o", obj])
     with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as pool:
         list(pool.map(lambda c: _run(c, verbose or ptxas_verbose), jobs))
     if force or jobs or _stale(LIB, objs):

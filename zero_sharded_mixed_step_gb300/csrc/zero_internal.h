@@ -60,6 +60,20 @@ constexpr int kErrSlots = 1024;
 // Which fused kernel a launch used (ZERO_VARIANT_VECTOR or ZERO_VARIANT_BULK).
 int last_fused_variant();
 
+// The rank-ordered fp32 mean of the W ranks' 16-bit gradients over
+// elements [lo, lo + len) of the flat vector, written to out[0, len).
+// lo must be a multiple of 8 and out 32-byte aligned.
+struct MeanLaunch {
+  int W;
+  int grad_dtype;
+  const void* grads[kMaxRanks];
+  int64_t lo, len;
+  float* out;
+  float inv_w;
+};
+
+cudaError_t launch_rank_mean(const MeanLaunch& a, cudaStream_t stream, int64_t* launches);
+
 // A byte range to copy, or a float range to cast.
 struct CopySeg {
   const void* src;
