@@ -570,7 +570,8 @@ int zero_offload_step(zero_offload* ctx, const void* const* grads, double lr, do
                       double eps, int64_t t);
 
 /* Cumulative figures of a context (any pointer may be NULL): the last step
- * counter, seconds the host spent in Adam, bytes copied device->host and
+ * counter, seconds of the steps' host phases (from the wait for the first
+ * chunk's mean to the last piece's update), bytes copied device->host and
  * host->device, kernels launched, host threads. */
 int zero_offload_stats(const zero_offload* ctx, int64_t* t, double* host_seconds, int64_t* d2h_bytes,
                        int64_t* h2d_bytes, int64_t* launches, int* threads);

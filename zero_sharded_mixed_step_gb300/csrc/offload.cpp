@@ -16,9 +16,11 @@
 //           16-bit copy, on a pool of threads;
 //   H2D     the chunk's 16-bit values into the device working copy (the
 //           all-gather, streamed).
-// The GPU and copy work for every chunk is enqueued up front; the host waits
-// for each chunk's mean to land, updates it, and enqueues its return copy, so
-// the copies of one chunk overlap the host arithmetic of its neighbours.
+// The GPU and copy work for every chunk is enqueued up front.  The host
+// threads then take pieces of the flat vector in order, with no barrier at
+// chunk boundaries: a chunk is updated as soon as its mean has landed, and
+// its return copy is enqueued as soon as its last piece is done, so the
+// copies of one chunk overlap the host arithmetic of its neighbours.
 //
 // The host arithmetic is the device kernel's operation for operation: fused
 // multiply-adds where the kernel fuses, separate products where it does not,
@@ -148,20 +150,26 @@ inline uint16_t to_fp16(float x) {
 }
 
 // Adam on [0, n) of the given arrays with mean gradient g; the order of
-// operations is that of the device kernel's element update.
+// operations is that of the device kernel's element update.  The recast runs
+// as a second loop over each tile of kTile elements (still in cache), so
+// that both loops vectorise at full width.
+constexpr int64_t kTile = 2048;
+
 template <bool BF16>
 void adam_range(const float* __restrict g, float* __restrict th, float* __restrict m, float* __restrict v,
                 uint16_t* __restrict out, int64_t n, const zero::AdamCoef c) {
-  for (int64_t i = 0; i < n; ++i) {
-    const float gi = g[i];
-    const float mi = std::fma(c.b1, m[i], c.omb1 * gi);
-    const float vi = std::fma(c.b2, v[i], (c.omb2 * gi) * gi);
-    const float den = std::fma(std::sqrt(vi), c.rsqrt_bc2, c.eps);
-    const float ti = th[i] - (c.step_size * mi) / den;
-    m[i] = mi;
-    v[i] = vi;
-    th[i] = ti;
-    out[i] = BF16 ? to_bf16(ti) : to_fp16(ti);
+  for (int64_t t0 = 0; t0 < n; t0 += kTile) {
+    const int64_t t1 = std::min(n, t0 + kTile);
+    for (int64_t i = t0; i < t1; ++i) {
+      const float gi = g[i];
+      const float mi = std::fma(c.b1, m[i], c.omb1 * gi);
+      const float vi = std::fma(c.b2, v[i], (c.omb2 * gi) * gi);
+      const float den = std::fma(std::sqrt(vi), c.rsqrt_bc2, c.eps);
+      m[i] = mi;
+      v[i] = vi;
+      th[i] = th[i] - (c.step_size * mi) / den;
+    }
+    for (int64_t i = t0; i < t1; ++i) out[i] = BF16 ? to_bf16(th[i]) : to_fp16(th[i]);
   }
 }
 
@@ -189,18 +197,39 @@ int64_t chunk_of(int64_t chunk_elems) {
   return (c + 7) / 8 * 8;
 }
 
-// Wait for an event with a deadline, sleeping between polls.
-int wait_event(cudaEvent_t e) {
+// Wait for an event with a deadline, sleeping between polls.  Returns
+// ZERO_OK, or an error code with *why set (nothing is recorded: the caller
+// may be a pool thread whose error message would not reach the user).
+int poll_event(cudaEvent_t e, const char** why) {
   const auto t0 = std::chrono::steady_clock::now();
   for (;;) {
     const cudaError_t r = cudaEventQuery(e);
     if (r == cudaSuccess) return ZERO_OK;
-    if (r != cudaErrorNotReady) return fail(ZERO_E_CUDA, cudaGetErrorString(r));
-    if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > kWaitSeconds)
-      return fail(ZERO_E_TIMEOUT, "a chunk's mean gradient did not reach host memory within 60 s");
+    if (r != cudaErrorNotReady) {
+      *why = cudaGetErrorString(r);
+      return ZERO_E_CUDA;
+    }
+    if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > kWaitSeconds) {
+      *why = "a chunk's mean gradient did not reach host memory within 60 s";
+      return ZERO_E_TIMEOUT;
+    }
     std::this_thread::sleep_for(std::chrono::microseconds(20));
   }
 }
+
+// The first error of a parallel phase (code and message), kept for the caller.
+struct FirstError {
+  std::atomic<int> code{ZERO_OK};
+  std::mutex mu;
+  std::string msg;
+  void note(int c, const char* m) {
+    int expected = ZERO_OK;
+    if (code.compare_exchange_strong(expected, c)) {
+      std::lock_guard<std::mutex> lk(mu);
+      msg = m;
+    }
+  }
+};
 
 }  // namespace
 
@@ -337,19 +366,55 @@ extern "C" int zero_offload_step(zero_offload* c, const void* const* grads, doub
     c->d2h_bytes += len * 4;
   }
   if (e != cudaSuccess) return fail(ZERO_E_CUDA, cudaGetErrorString(e));
-  // the host half, chunk by chunk as the means land
+  // The host half.  Every host thread takes pieces of kGrain elements in flat
+  // order, with no barrier between chunks: the first thread to reach a chunk
+  // waits for its mean to land, and the thread that finishes a chunk's last
+  // piece sends the chunk's 16-bit values back to the device.
+  const int64_t per_chunk = (c->chunk + kGrain - 1) / kGrain;
+  const int64_t last_len = c->n_pad - (c->n_chunks - 1) * c->chunk;
+  const int64_t pieces = c->n_chunks > 0 ? (c->n_chunks - 1) * per_chunk + (last_len + kGrain - 1) / kGrain : 0;
+  std::vector<std::atomic<int>> ready(c->n_chunks);
+  std::vector<std::atomic<int64_t>> left(c->n_chunks);
   for (int64_t k = 0; k < c->n_chunks; ++k) {
-    const int64_t lo = k * c->chunk, len = std::min(c->chunk, c->n_pad - lo);
-    if ((rc = wait_event(c->landed[k]))) return rc;
-    const auto t0 = std::chrono::steady_clock::now();
-    adam_parallel(*c->pool, c->host_grad + lo, c->master + lo, c->m + lo, c->v + lo, c->host_p16 + lo, len, coef,
-                  c->work_dtype);
-    c->host_seconds += std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
-    e = cudaMemcpyAsync(static_cast<uint16_t*>(c->p16) + lo, c->host_p16 + lo, len * 2, cudaMemcpyHostToDevice,
-                        c->h2d);
-    if (e != cudaSuccess) return fail(ZERO_E_CUDA, cudaGetErrorString(e));
-    c->h2d_bytes += len * 2;
+    ready[k].store(0);
+    const int64_t len = std::min(c->chunk, c->n_pad - k * c->chunk);
+    left[k].store((len + kGrain - 1) / kGrain);
   }
+  FirstError err;
+  uint16_t* const dev16 = static_cast<uint16_t*>(c->p16);
+  const auto t0 = std::chrono::steady_clock::now();
+  c->pool->run(pieces, 1, [&](int64_t p0, int64_t p1) {
+    for (int64_t p = p0; p < p1; ++p) {
+      if (err.code.load() != ZERO_OK) return;
+      const int64_t k = p / per_chunk;
+      const int64_t clo = k * c->chunk, clen = std::min(c->chunk, c->n_pad - clo);
+      const int64_t lo = clo + (p % per_chunk) * kGrain, hi = std::min(clo + clen, lo + kGrain);
+      if (!ready[k].load(std::memory_order_acquire)) {
+        const char* why = "";
+        const int rc2 = poll_event(c->landed[k], &why);
+        if (rc2 != ZERO_OK) {
+          err.note(rc2, why);
+          return;
+        }
+        ready[k].store(1, std::memory_order_release);
+      }
+      if (c->work_dtype == ZERO_BF16)
+        adam_range<true>(c->host_grad + lo, c->master + lo, c->m + lo, c->v + lo, c->host_p16 + lo, hi - lo, coef);
+      else
+        adam_range<false>(c->host_grad + lo, c->master + lo, c->m + lo, c->v + lo, c->host_p16 + lo, hi - lo, coef);
+      if (left[k].fetch_sub(1) == 1) {
+        const cudaError_t e2 =
+            cudaMemcpyAsync(dev16 + clo, c->host_p16 + clo, clen * 2, cudaMemcpyHostToDevice, c->h2d);
+        if (e2 != cudaSuccess) {
+          err.note(ZERO_E_CUDA, cudaGetErrorString(e2));
+          return;
+        }
+      }
+    }
+  });
+  c->host_seconds += std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+  if (err.code.load() != ZERO_OK) return fail(err.code.load(), err.msg);
+  c->h2d_bytes += c->n_pad * 2;
   // later work on the caller's stream sees the new working copy
   e = cudaEventRecord(c->returned, c->h2d);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(c->stream, c->returned, 0);
