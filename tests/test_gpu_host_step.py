@@ -1,6 +1,8 @@
 """zero_step_host: the step fed from host memory through the staging ring,
 against zero_step on the same gradients (GPU needed)."""
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -97,14 +99,19 @@ def test_host_step_equals_device_step(case):
 
 
 def test_host_alloc_is_page_locked_aligned_and_zeroed():
-    """zero_host_alloc: the memory starts on a huge-page boundary, reads as
+    """zero_host_alloc: a block of a huge page or more starts on a huge-page
+    boundary (a small one on a page boundary), reads as
     zeros, counts as page-locked for CUDA copies, and is returned by
     zero_host_free (twice is an error: the address is no longer known)."""
     try:
         huge = int(open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size").read())
     except OSError:
         huge = 2 << 20
-    buf = zs.HostBuffer((3 << 20) + 5, torch.float16)
+    page = os.sysconf("SC_PAGE_SIZE")
+    small = zs.HostBuffer(1000, torch.float32)
+    assert small.ptr % page == 0 and small.tensor.is_pinned()
+    small.close()
+    buf = zs.HostBuffer(huge // 2 + 5, torch.float16)      # just over one huge page of bytes
     assert buf.ptr % huge == 0
     assert buf.tensor.is_pinned()
     assert int(buf.tensor.view(torch.int16).abs().max()) == 0

@@ -77,19 +77,24 @@ extern "C" int zero_host_alloc(int64_t bytes, void** out) {
   const size_t huge = huge_page_bytes();
   const long page_l = sysconf(_SC_PAGESIZE);
   const size_t page = page_l > 0 ? static_cast<size_t>(page_l) : 4096;
-  const size_t len = (static_cast<size_t>(bytes) + huge - 1) / huge * huge;
-  const size_t map_len = len + huge;   // room to start on a huge-page boundary
+  const size_t len = (static_cast<size_t>(bytes) + page - 1) / page * page;
+  // Blocks of at least one huge page start on a huge-page boundary (the
+  // mapping has room for the shift) so that every whole huge page inside can
+  // be one; smaller blocks stay on base pages and waste nothing.
+  const bool use_huge = len >= huge;
+  const size_t map_len = use_huge ? len + huge : len;
   void* base = mmap(nullptr, map_len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
   if (base == MAP_FAILED) return fail(ZERO_E_NOMEM, std::string("mmap failed: ") + std::strerror(errno));
-  char* p = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(base) + huge - 1) / huge * huge);
+  char* p = use_huge ? reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(base) + huge - 1) / huge * huge)
+                     : static_cast<char*>(base);
 #ifdef MADV_HUGEPAGE
-  madvise(p, len, MADV_HUGEPAGE);   // advice only: where huge pages are off, base pages serve
+  if (use_huge) madvise(p, len, MADV_HUGEPAGE);   // advice only: where huge pages are off, base pages serve
 #endif
-  populate(p, len, page, huge);
+  populate(p, len, page, use_huge ? huge : (size_t(2) << 20));
 #ifdef MADV_COLLAPSE
   // where the first touches got base pages (no free huge page at that
   // moment), ask the kernel to compact and collapse them now; advice only
-  madvise(p, len, MADV_COLLAPSE);
+  if (use_huge) madvise(p, len, MADV_COLLAPSE);
 #endif
   const cudaError_t e = cudaHostRegister(p, len, cudaHostRegisterDefault);
   if (e != cudaSuccess) {
