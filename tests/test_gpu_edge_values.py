@@ -1,0 +1,80 @@
+"""Degenerate values through every step entry point (GPU needed): masters
+beyond the fp16 range (the working copy becomes +-inf, reading 5), gradients
+at the fp16 maximum, and all-zero gradients (nothing may move).  The device
+step, DP with literal replicas and the offloaded step must agree bit for bit
+and stay within the tolerance of the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import zero_sharded_mixed_step_gb300 as zs
+from oracle import zero_oracle as z
+from tests.gpu_harness import assert_16bit_band, assert_f32_close, bits_of
+
+pytestmark = pytest.mark.gpu
+
+W = 4
+HP = (1e-2, 0.9, 0.999, 1e-8)
+
+
+def _theta0():
+    edge = np.array([65503.0, 65519.99, 65520.0, 65536.0, 70000.0, -70000.0, 1e6, -65504.0, 65504.0, 0.0,
+                     6e-8, -6e-8, 1e-30], np.float32)
+    rng = np.random.default_rng(5)
+    return np.concatenate([edge, (rng.standard_normal(1000) * 0.02).astype(np.float32)])
+
+
+def _grads(theta0, kind, t):
+    n = theta0.size
+    rng = np.random.default_rng(100 + t)
+    if kind == "zero":
+        g = np.zeros((W, n), np.float32)
+    elif kind == "fp16max":
+        g = np.where(rng.random((W, n)) < 0.5, -65504.0, 65504.0).astype(np.float32)
+    else:
+        g = (rng.standard_normal((W, n)) * 1e-3).astype(np.float32)
+        g[:, :13] = -1.0        # push the edge masters upwards
+    return [torch.from_numpy(x).to(torch.float16) for x in g]
+
+
+@pytest.mark.parametrize("kind", ["normal", "fp16max", "zero"])
+def test_edge_values_agree_everywhere(kind):
+    theta0 = _theta0()
+    n = theta0.size
+    dev = zs.ZeroStep(zs.ZERO_SCHEME_Z2, W, [n], "fp16", "fp16", theta0=torch.from_numpy(theta0), device="cuda")
+    rep = zs.DpReplicas(W, n, "fp16", "fp16", theta0=torch.from_numpy(theta0).cuda(), device="cuda")
+    off = zs.ZeroOffload(W, n, "fp16", "fp16", theta0=torch.from_numpy(theta0), threads=2, chunk_elems=256)
+    orc = z.SingleReplica(theta0.copy(), "fp16")
+    grads = dev.new_grad_buffers()
+    for t in range(1, 4):
+        draws = _grads(theta0, kind, t)
+        for g, d in zip(grads, draws):
+            g[:n].copy_(d)
+        dev.step(grads, *HP, t)
+        rep.step(grads, *HP, t)
+        off.step(grads, *HP, t)
+        orc.step([d.numpy() for d in draws], *HP)
+        torch.cuda.synchronize()
+        th = dev.master[:n].cpu().numpy()
+        assert_f32_close(th, orc.master, f"{kind} t={t} master")
+        p16 = bits_of(dev.p16[:n])
+        assert_16bit_band(p16, orc.master, "fp16", f"{kind} t={t} working copy")
+        assert np.array_equal(p16, bits_of(dev.master[:n].to(torch.float16)))
+        for r in range(W):
+            assert torch.equal(rep.master[r].view(torch.int32), dev.master.view(torch.int32))
+            assert torch.equal(rep.p16[r].view(torch.int16), dev.p16.view(torch.int16))
+        assert torch.equal(off.master.view(torch.int32), dev.master.cpu().view(torch.int32))
+        assert torch.equal(off.p16.view(torch.int16), dev.p16.view(torch.int16))
+    final = dev.master[:n].cpu().numpy()
+    wc = bits_of(dev.p16[:n])
+    # beyond the fp16 range the working copy is infinite, with the master's sign
+    big = np.abs(final) >= 65520.0
+    assert big.sum() >= 4
+    assert np.all(wc[big & (final > 0)] == 0x7C00) and np.all(wc[big & (final < 0)] == 0xFC00)
+    if kind == "zero":
+        assert np.array_equal(final.view(np.uint32), theta0.view(np.uint32))
+        assert bool((dev.m == 0).all()) and bool((dev.v == 0).all())
+    assert rep.mismatches() == 0
+    off.close()
+    dev.close()
