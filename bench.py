@@ -210,6 +210,25 @@ class ClockSampler:
 
 # ---- the CPU oracle (the CPU baseline leg and the reference arm) --------------------
 
+def oracle_bytes(wl, elems: int) -> int:
+    """Host bytes the oracle holds for a sample of ``elems`` parameters: W
+    16-bit gradient vectors and their fp64 copies, fp32 master / m / v per
+    rank copy (W of them under literal DP replicas), and fp64 temporaries."""
+    copies = wl.W if scheme_of(wl) == 0 else 1
+    return elems * (wl.W * (2 + 8) + copies * (12 + 2) + 6 * 8)
+
+
+def check_host_memory(need: int, what: str) -> None:
+    """Fail with a clear message, before allocating, when the host cannot hold ``need`` bytes."""
+    try:
+        with open("/proc/meminfo") as f:
+            avail = next(int(line.split()[1]) * 1024 for line in f if line.startswith("MemAvailable:"))
+    except (OSError, StopIteration):
+        return
+    if need > avail:
+        raise MemoryError(f"{what} needs about {need / 1e9:.1f} GB of host memory; {avail / 1e9:.1f} GB available")
+
+
 def oracle_sample_step_seconds(wl, sample_elems: int, dtype: str):
     """Seconds the oracle takes for one step of ``wl`` restricted to a sample
     of about ``sample_elems`` parameters (ZeRO-3: whole units shrunk to that
@@ -220,6 +239,7 @@ def oracle_sample_step_seconds(wl, sample_elems: int, dtype: str):
     scheme = scheme_of(wl)
     W = wl.W
     sample_elems = max(W, sample_elems // W * W)
+    check_host_memory(oracle_bytes(wl, sample_elems), f"the CPU oracle on {sample_elems:,} parameters")
     units = [sample_elems] if scheme != 3 else [min(sample_elems, wl.units()[0])]
     small = wk.scaled(wl, unit_sizes=units, name=wl.name + "_sample") if scheme == 3 else \
         wk.scaled(wl, n=sample_elems, name=wl.name + "_sample")

@@ -5,8 +5,10 @@
  * Adam on every parameter: at t = 1, m_hat = g and v_hat = g^2, so each
  * parameter moves by -lr g / (|g| + eps) - by lr sign(g) up to
  * lr eps / (|g| + eps) - and not at all where g = 0.  It also checks that an
- * out-of-order step counter is refused with ZERO_E_STATE.  Exit status 0 on
- * success.
+ * out-of-order step counter is refused with ZERO_E_STATE, and runs the same
+ * step with the optimizer on the host (zero_offload_*, link buffers from
+ * zero_host_alloc), which must give the same master bit for bit.  Exit
+ * status 0 on success.
  */
 #include <math.h>
 #include <stdint.h>
@@ -109,6 +111,34 @@ int main(void) {
   }
   CHECK(bad == 0, "%d parameters violate the first-step closed form", bad);
   CHECK(zero_destroy(ctx) == ZERO_OK, "destroy: %s", zero_last_error());
-  printf("c client: ZeRO-2 first step of %lld parameters on %d ranks matches the closed form\n", (long long)n, W);
+
+  /* The same step with the optimizer on the host: fp32 state in malloc'd
+   * memory, the link buffers from zero_host_alloc; bit-identical master. */
+  float* o_master = calloc((size_t)n_pad, sizeof(float));
+  float* o_m = calloc((size_t)n_pad, sizeof(float));
+  float* o_v = calloc((size_t)n_pad, sizeof(float));
+  memcpy(o_master, h_theta, (size_t)n_pad * sizeof(float));
+  void *o_grad = NULL, *o_p16 = NULL, *d_p16 = NULL, *staging = NULL;
+  CHECK(zero_host_alloc(n_pad * 4, &o_grad) == ZERO_OK, "host alloc: %s", zero_last_error());
+  CHECK(zero_host_alloc(n_pad * 2, &o_p16) == ZERO_OK, "host alloc: %s", zero_last_error());
+  const int64_t chunk = 64; /* many chunks, to exercise the pipeline */
+  const int64_t sbytes = zero_offload_staging_bytes(chunk);
+  CHECK(cudaMalloc(&d_p16, n_pad * 2) == cudaSuccess, "cudaMalloc");
+  CHECK(cudaMalloc(&staging, sbytes) == cudaSuccess, "cudaMalloc");
+  zero_offload* off = NULL;
+  CHECK(zero_offload_init(&off, W, n, ZERO_BF16, ZERO_BF16, o_master, o_m, o_v, (float*)o_grad, o_p16, d_p16,
+                          staging, sbytes, chunk, 3, NULL) == ZERO_OK,
+        "offload init: %s", zero_last_error());
+  CHECK(zero_offload_step(off, (const void* const*)grads, lr, b1, b2, eps, 1) == ZERO_OK, "offload step: %s",
+        zero_last_error());
+  CHECK(cudaDeviceSynchronize() == cudaSuccess, "sync");
+  CHECK(memcmp(o_master, h_out, (size_t)n_pad * sizeof(float)) == 0, "offloaded master differs from ZeRO-2");
+  uint16_t* dev_copy = malloc((size_t)n_pad * 2);
+  cudaMemcpy(dev_copy, d_p16, n_pad * 2, cudaMemcpyDeviceToHost);
+  CHECK(memcmp(dev_copy, o_p16, (size_t)n_pad * 2) == 0, "device working copy differs from the host's");
+  CHECK(zero_offload_destroy(off) == ZERO_OK, "offload destroy");
+  CHECK(zero_host_free(o_grad) == ZERO_OK && zero_host_free(o_p16) == ZERO_OK, "host free");
+  printf("c client: ZeRO-2 first step of %lld parameters on %d ranks matches the closed form; "
+         "the host-offloaded step gives the same bits\n", (long long)n, W);
   return 0;
 }

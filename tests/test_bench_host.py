@@ -76,3 +76,16 @@ def test_reference_arm_prints_the_contract_line(monkeypatch):
     assert line["impl"] == "reference" and line["unit"] == "params/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["metric"] == bench.METRIC
+
+
+def test_oracle_host_memory_check_refuses_what_does_not_fit(monkeypatch):
+    """The CPU oracle's host-memory check: a sample that fits passes, one that
+    needs more than the host has fails with a message before allocating."""
+    import bench
+    import workloads as wk
+    wl = wk.GPT2_XL
+    bench.check_host_memory(bench.oracle_bytes(wl, 1 << 16), "small sample")
+    with pytest.raises(MemoryError, match="host memory"):
+        bench.check_host_memory(bench.oracle_bytes(wl, wl.n) * 1000, "the whole GPT-2-1.5B vector, 1000 times")
+    # literal DP replicas cost the oracle W copies of the state
+    assert bench.oracle_bytes(wk.GPT2_SMALL_DP_REPLICAS, 1000) > bench.oracle_bytes(wk.GPT2_SMALL, 1000)
