@@ -47,6 +47,10 @@
  * zero_refresh_working_copy enqueue work on the context's streams and return
  * without waiting; zero_sync waits (with a deadline), and zero_get_state /
  * zero_set_state wait for their own copies.
+ *
+ * Threads.  A context (zero_ctx, zero_offload) is used by one host thread at
+ * a time; different contexts may be used from different threads at once.
+ * Error messages are kept per thread.
  */
 #ifndef ZERO_STEP_H
 #define ZERO_STEP_H
@@ -565,7 +569,10 @@ int zero_offload_init(zero_offload** out, int W, int64_t n, int grad_dtype, int 
  * step counter (ZERO_E_STATE otherwise).  The call returns when the host
  * update is done; the copies of the new working copy may still be in
  * flight, and work enqueued later on `stream` runs after them.  A chunk whose
- * mean has not reached host memory within 60 s gives ZERO_E_TIMEOUT.
+ * mean has not reached host memory within 60 s gives ZERO_E_TIMEOUT.  An
+ * error after the argument checks (ZERO_E_CUDA, ZERO_E_TIMEOUT) can leave
+ * the host state and the working copy partly updated and the step counter
+ * unchanged: restore master, m and v from a saved copy before going on.
  */
 int zero_offload_step(zero_offload* ctx, const void* const* grads, double lr, double beta1, double beta2,
                       double eps, int64_t t);

@@ -112,3 +112,12 @@ def test_offload_init_checks_before_any_cuda_call(zlib):
     assert _err(init, 4, 100, 0, 0, *ok[:6], fake(11) + 16, *ok[7:]) == zs.ZERO_E_ALIGN
     assert _err(init, 4, 100, 0, 0, *ok[:7], need - 1, 1000) == zs.ZERO_E_ARG
     assert _err(init, 4, 100, 0, 0, h[0] + 1, *ok[1:]) == zs.ZERO_E_ALIGN
+
+
+def test_offload_init_refuses_overlapping_host_buffers(zlib):
+    need = zs.zero_offload_staging_bytes(1000)
+    h = [fake(k) for k in range(5)]
+    # m inside master
+    assert _err(zs.zero_offload_init, 4, 100, 0, 0, h[0], h[0] + 64, h[2], h[3], h[4], fake(10), fake(11), need,
+                1000) == zs.ZERO_E_ARG
+    assert "overlap" in zs.zero_last_error()

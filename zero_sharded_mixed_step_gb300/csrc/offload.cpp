@@ -43,6 +43,7 @@
 #include <mutex>
 #include <string>
 #include <thread>
+#include <utility>
 #include <vector>
 
 #include "zero_internal.h"
@@ -290,6 +291,18 @@ extern "C" int zero_offload_init(zero_offload** out, int W, int64_t n, int grad_
   const int64_t chunk = chunk_of(chunk_elems);
   if (staging_bytes < zero_offload_staging_bytes(chunk_elems))
     return fail(ZERO_E_ARG, "staging is smaller than zero_offload_staging_bytes(chunk_elems)");
+  {
+    // the host buffers are all written: none may share memory with another
+    const uintptr_t np = static_cast<uintptr_t>((n + W - 1) / W * W);
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    for (const void* p : {static_cast<const void*>(host_master), static_cast<const void*>(host_m),
+                          static_cast<const void*>(host_v), static_cast<const void*>(host_grad)})
+      r.emplace_back(reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + 4 * np);
+    r.emplace_back(reinterpret_cast<uintptr_t>(host_p16), reinterpret_cast<uintptr_t>(host_p16) + 2 * np);
+    std::sort(r.begin(), r.end());
+    for (size_t k = 1; k < r.size(); ++k)
+      if (np > 0 && r[k].first < r[k - 1].second) return fail(ZERO_E_ARG, "host buffers overlap one another");
+  }
   auto* c = new zero_offload;
   c->W = W;
   c->n = n;
