@@ -471,11 +471,12 @@ def run_ours(args):
         # host buffers from zero_host_alloc: page-locked on huge pages, where the
         # link holds its full rate (memory from cudaHostAlloc measured slower)
         host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in step.grads]
-        host_grads = [b.tensor for b in host_bufs]
-        for h, g in zip(host_grads, step.grads):
-            h.copy_(g)
         out_elems = step.n_pad if scheme != 3 else wl.W * step.sizes["shard_store"]
         host_bufs.append(zs.HostBuffer(out_elems, step.work_torch_dtype))
+        huge_at_alloc = huge_page_fraction(host_bufs)
+        host_grads = [b.tensor for b in host_bufs[:-1]]
+        for h, g in zip(host_grads, step.grads):
+            h.copy_(g)
         host_out = host_bufs[-1].tensor
         need = zs.zero_host_staging_bytes(scheme, wl.W, units, 0)
         staging = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -493,6 +494,7 @@ def run_ours(args):
             back = [(host_out[r * S16:(r + 1) * S16], step.shard16[r]) for r in range(wl.W)]
         link = link_probe(list(zip(step.grads, host_grads)), back, sh)
         link["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
+        link["host_huge_page_fraction_at_alloc"] = huge_at_alloc
         for _ in range(2):               # warm the path, untimed
             host_step()
         step.sync()

@@ -302,8 +302,10 @@ int zero_step_host(zero_ctx* ctx, int scheme, int W, int64_t n, const void* cons
  * Measured on GB300 hosts,
  * 1 GB copies out of memory pinned with cudaHostAlloc ran from 38 to 212
  * GB/s, slower in later processes on the same host, while copies out of
- * this memory held 208-212 GB/s.  A block of at least one huge page starts
- * on a huge-page boundary; a smaller one on a page boundary, on base pages.
+ * this memory held 208-212 GB/s.  A block of at least one huge page is
+ * mapped as whole huge pages from a huge-page boundary (its last page may
+ * extend past `bytes`); a smaller one starts on a page boundary, on base
+ * pages.
  * The contents are zero.  *out receives the address (NULL on
  * failure).  The memory is the caller's until zero_host_free.
  * ZERO_E_ARG for bytes <= 0 or out NULL; ZERO_E_NOMEM if the mapping

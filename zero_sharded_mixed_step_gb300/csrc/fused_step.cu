@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -224,6 +225,7 @@ constexpr int kTile = 2048;
 constexpr int kStages = 2;
 constexpr int kBulkThreads = kTile / 8;
 constexpr long long kWaitCycles = 1LL << 31;
+constexpr int64_t kBulkMinTilesPerCta = 8;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -445,20 +447,21 @@ cudaError_t launch_fused_step(const FusedLaunch& a, cudaStream_t stream, int64_t
     aligned = aligned && vec16_host(a.segs[s].out, a.segs[s].lo) && (!pre || vec16_host(a.segs[s].pre_out, a.segs[s].lo));
   }
   // The bulk-staged kernel needs a compile-time W and 16-byte aligned 16-bit
-  // slots.  Left to choose, it is used where it measured faster: W of 8 or 16
-  // and at least one whole tile.
+  // slots.  Left to choose, it is used where it measured no slower: W of 8 or
+  // 16 and at least kBulkMinTilesPerCta tiles for each CTA (with fewer, the
+  // ring's fill and drain dominate: at 2^20 elements the register kernel
+  // took 15 us against 17).
   const BulkKernel bulk = pre ? pick_bulk_t<true>(a.grad_dtype, a.work_dtype, a.W)
                               : pick_bulk_t<false>(a.grad_dtype, a.work_dtype, a.W);
   const bool bulk_ok = bulk.fn != nullptr && aligned && a.variant != ZERO_VARIANT_VECTOR;
+  const int64_t bulk_ctas = (static_cast<int64_t>(sm_count()) + a.nseg - 1) / a.nseg;   // one CTA per SM in all
+  const int64_t tiles = longest / kTile;
   const bool use_bulk =
-      bulk_ok && (a.variant == ZERO_VARIANT_BULK || (a.W >= 8 && longest >= kTile));
+      bulk_ok && (a.variant == ZERO_VARIANT_BULK || (a.W >= 8 && tiles >= kBulkMinTilesPerCta * bulk_ctas));
   if (use_bulk) {
     cudaError_t err = cudaFuncSetAttribute(bulk.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bulk.smem);
     if (err != cudaSuccess) return err;
-    int64_t bx = (static_cast<int64_t>(sm_count()) + a.nseg - 1) / a.nseg;   // one CTA per SM in all
-    const int64_t tiles = longest / kTile;
-    if (bx > tiles) bx = tiles;
-    if (bx < 1) bx = 1;
+    const int64_t bx = std::max<int64_t>(1, std::min(bulk_ctas, tiles));
     dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(a.nseg));
     bulk.fn<<<grid, kBulkThreads, bulk.smem, stream>>>(a);
     ++*launches;

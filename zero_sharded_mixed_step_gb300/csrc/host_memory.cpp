@@ -77,11 +77,13 @@ extern "C" int zero_host_alloc(int64_t bytes, void** out) {
   const size_t huge = huge_page_bytes();
   const long page_l = sysconf(_SC_PAGESIZE);
   const size_t page = page_l > 0 ? static_cast<size_t>(page_l) : 4096;
-  const size_t len = (static_cast<size_t>(bytes) + page - 1) / page * page;
-  // Blocks of at least one huge page start on a huge-page boundary (the
-  // mapping has room for the shift) so that every whole huge page inside can
-  // be one; smaller blocks stay on base pages and waste nothing.
-  const bool use_huge = len >= huge;
+  // Blocks of at least one huge page are whole huge pages, starting on a
+  // huge-page boundary (the mapping has room for the shift), so that no part
+  // of them is left on base pages; smaller blocks stay on base pages and
+  // waste nothing.
+  const bool use_huge = static_cast<size_t>(bytes) >= huge;
+  const size_t unit = use_huge ? huge : page;
+  const size_t len = (static_cast<size_t>(bytes) + unit - 1) / unit * unit;
   const size_t map_len = use_huge ? len + huge : len;
   void* base = mmap(nullptr, map_len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
   if (base == MAP_FAILED) return fail(ZERO_E_NOMEM, std::string("mmap failed: ") + std::strerror(errno));
