@@ -19,14 +19,14 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libzero_gb300.so")
-SOURCES = ["zero_api.cpp", "fused_step.cu", "copy_cast.cu", "zero3_static.cu", "dp_replicas.cu",
+SOURCES = ["zero_api.cpp", "host_step.cpp", "bucket_step.cpp", "fused_step.cu", "copy_cast.cu", "zero3_static.cu", "dp_replicas.cu",
            "host_memory.cpp", "offload_mean.cu", "offload.cpp"]
 # Host arithmetic must match the device kernel's operation for operation: no
 # contraction of a product and a sum into one fused operation by the compiler
 # (the code writes every fused multiply-add it wants), and no errno from sqrt,
 # which would keep the loop from being vectorised.
 EXTRA_FLAGS = {"offload.cpp": ["-Xcompiler", "-ffp-contract=off", "-Xcompiler", "-fno-math-errno"]}
-HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "step_math.cuh"),
+HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "zero_context.h"), os.path.join(CSRC, "step_math.cuh"),
            os.path.join(INCLUDE, "zero_step.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,24 +1,26 @@
 // Host side of libzero_gb300: argument checks, layout and accounting, the
 // context, and the ZeRO-3 unit scheduler that drives the kernels on CUDA
-// streams.  See include/zero_step.h for the contract of every entry point.
+// streams.  The step fed from host memory is in host_step.cpp and the
+// bucketed step in bucket_step.cpp.  See include/zero_step.h for the
+// contract of every entry point.
 
 #include "zero_step.h"
 
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <algorithm>
 #include <chrono>
 #include <cmath>
-#include <mutex>
 #include <cstdarg>
 #include <cstdio>
-#include <algorithm>
 #include <cstring>
-#include <map>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <vector>
 
+#include "zero_context.h"
 #include "zero_internal.h"
 
 static_assert(ZERO_MAX_RANKS == zero::kMaxRanks, "rank limit must match the kernels'");
@@ -26,6 +28,11 @@ static_assert(ZERO_MAX_RANKS == zero::kMaxRanks, "rank limit must match the kern
 namespace {
 
 thread_local std::string g_last_error;
+
+}  // namespace
+
+namespace zero {
+namespace host {
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -40,43 +47,6 @@ int fail(int code, const char* fmt, ...) {
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(ZERO_E_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
-
-#define ZERO_CUDA(call)                                 \
-  do {                                                  \
-    cudaError_t e_ = (call);                            \
-    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
-  } while (0)
-
-// NVTX range on the host timeline (a no-op unless a profiler is attached)
-struct Range {
-  explicit Range(const char* name) { nvtxRangePushA(name); }
-  Range(const char* fmt, long long a) {
-    char buf[96];
-    snprintf(buf, sizeof buf, fmt, a);
-    nvtxRangePushA(buf);
-  }
-  ~Range() { nvtxRangePop(); }
-  Range(const Range&) = delete;
-  Range& operator=(const Range&) = delete;
-};
-
-constexpr uint16_t kPoison16 = 0x7FFF;   // a NaN in both fp16 and bf16
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-// master, m and v are read and written 32 bytes at a time
-bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
-
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-bool valid_scheme(int s) { return s >= ZERO_SCHEME_DP && s <= ZERO_SCHEME_Z3; }
-bool valid_dtype(int d) { return d == ZERO_FP16 || d == ZERO_BF16; }
-
-// Flat padded layout of the units ("ZeRO and FSDP": even split, zero padding
-// to a multiple of W; each unit split on its own for ZeRO-3).
-struct Layout {
-  std::vector<int64_t> size, off, shard, off16;
-  int64_t n = 0, n_pad = 0, shard_total = 0, unit_max = 0;
-};
 
 int make_layout(int W, int64_t n_units, const int64_t* sizes, Layout* L) {
   if (W < 1 || W > ZERO_MAX_RANKS) return fail(ZERO_E_ARG, "W=%d outside [1, %d]", W, ZERO_MAX_RANKS);
@@ -101,84 +71,6 @@ int make_layout(int W, int64_t n_units, const int64_t* sizes, Layout* L) {
   return ZERO_OK;
 }
 
-int64_t resident_bytes(int scheme, int64_t n, int64_t S) {
-  // bands: 2 (16-bit weight) + 2 (16-bit gradient) + 12 (fp32 master, m, v)
-  const bool so = scheme >= ZERO_SCHEME_Z1, sg = scheme >= ZERO_SCHEME_Z2, sp = scheme >= ZERO_SCHEME_Z3;
-  return 2 * (sp ? S : n) + 2 * (sg ? S : n) + 12 * (so ? S : n);
-}
-
-// Bytes one rank sends in one ring reduce-scatter or all-gather of a unit
-// whose shard is S values of 2 bytes: W - 1 chunks ("One Poem Suffices:
-// ZeRO", appendix B).
-int64_t ring_bytes(int W, int64_t S) { return int64_t(W - 1) * S * 2; }
-
-// Counter slots for bounded device waits: slot 0 belongs to no context, the
-// others are handed to contexts while they live; when all are taken, new
-// contexts share the last one.
-std::mutex g_slot_mu;
-bool g_slot_used[zero::kErrSlots] = {true};
-
-int take_slot() {
-  std::lock_guard<std::mutex> lock(g_slot_mu);
-  for (int i = 1; i < zero::kErrSlots; ++i)
-    if (!g_slot_used[i]) {
-      g_slot_used[i] = true;
-      return i;
-    }
-  return zero::kErrSlots - 1;
-}
-
-void give_slot(int i) {
-  std::lock_guard<std::mutex> lock(g_slot_mu);
-  if (i > 0 && i < zero::kErrSlots - 1) g_slot_used[i] = false;
-}
-
-}  // namespace
-
-int zero::record_error(int code, const char* msg) { return fail(code, "%s", msg); }
-
-struct zero_ctx {
-  int scheme = 0, W = 0, gdt = 0, wdt = 0;
-  Layout L;
-  float* master = nullptr;
-  float* m = nullptr;
-  float* v = nullptr;
-  void* p16 = nullptr;
-  std::vector<void*> shard16;
-  void* ubuf[2] = {nullptr, nullptr};
-  cudaStream_t su = nullptr, sg = nullptr;
-  bool cuda_ready = false;
-  cudaEvent_t ev_begin = nullptr, ev_gathered[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
-  cudaEvent_t ev_landed[2] = {nullptr, nullptr}, ev_slot_free[2] = {nullptr, nullptr};
-  cudaEvent_t ev_updated[2] = {nullptr, nullptr}, ev_out_done = nullptr;
-  std::vector<cudaStream_t> touched;
-  int variant = ZERO_VARIANT_AUTO;
-  int64_t t = 0;
-  int64_t comm = 0, launches = 0, gathers = 0, scatters = 0, live_elems = 0, peak_live = 0;
-  std::vector<char> live;
-  std::vector<char> rank_up;
-  zero_unit_hook hook = nullptr;
-  void* hook_user = nullptr;
-  bool timing = false;
-  bool stall_pending = false;
-  int64_t stall_tile = -1;
-  int err_slot = 0;            // this context's device error counter slot
-  bool err_slot_ready = false; // cleared on the device (at the first fused launch)
-  int64_t dev_err_seen = 0;    // count at the last zero_sync
-  int last_variant = 0;
-  // a step being done bucket by bucket: the ranges covered so far (lo -> hi)
-  int debug = 0;
-  std::vector<void*> live_buf;          // where the caller gathered each live unit
-  std::vector<cudaStream_t> live_stream;
-  bool bucket_open = false;
-  std::map<int64_t, int64_t> covered;
-  int64_t covered_elems = 0;
-  std::vector<cudaEvent_t> event_pool;
-  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[3];
-};
-
-namespace {
-
 int ensure_cuda(zero_ctx* c) {
   if (c->cuda_ready) return ZERO_OK;
   ZERO_CUDA(cudaEventCreateWithFlags(&c->ev_begin, cudaEventDisableTiming));
@@ -194,7 +86,6 @@ int ensure_cuda(zero_ctx* c) {
   return ZERO_OK;
 }
 
-// Timing brackets: an event before and after a launch, on its stream.
 int take_event(zero_ctx* c, cudaEvent_t* e) {
   if (!c->event_pool.empty()) {
     *e = c->event_pool.back();
@@ -204,27 +95,6 @@ int take_event(zero_ctx* c, cudaEvent_t* e) {
   ZERO_CUDA(cudaEventCreate(e));
   return ZERO_OK;
 }
-
-struct Bracket {
-  zero_ctx* c;
-  int kind;
-  cudaStream_t s;
-  cudaEvent_t a = nullptr, b = nullptr;
-  int open() {
-    if (!c->timing) return ZERO_OK;
-    int rc = take_event(c, &a);
-    if (rc == ZERO_OK) rc = take_event(c, &b);
-    if (rc) return rc;
-    ZERO_CUDA(cudaEventRecord(a, s));
-    return ZERO_OK;
-  }
-  int close() {
-    if (!c->timing) return ZERO_OK;
-    ZERO_CUDA(cudaEventRecord(b, s));
-    c->timed[kind].push_back({a, b});
-    return ZERO_OK;
-  }
-};
 
 void touch(zero_ctx* c, cudaStream_t s) {
   for (cudaStream_t x : c->touched)
@@ -284,7 +154,7 @@ zero::AdamCoef make_coef(double lr, double b1, double b2, double eps, int64_t t,
 // For DP/Z1/Z2, [lo, lo + len) limits the pass to part of the flat vector
 // (len < 0: all of it).
 int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const zero::AdamCoef& coef,
-                  cudaStream_t stream, void* gather_dst = nullptr, int64_t lo = 0, int64_t len = -1) {
+                  cudaStream_t stream, void* gather_dst, int64_t lo, int64_t len) {
   zero::FusedLaunch a;
   std::memset(&a, 0, sizeof a);
   a.W = c->W;
@@ -365,6 +235,42 @@ void count_scatter(zero_ctx* c, int64_t u) {
 void live_add(zero_ctx* c, int64_t elems) {
   c->live_elems += elems;
   if (c->live_elems > c->peak_live) c->peak_live = c->live_elems;
+}
+
+}  // namespace host
+}  // namespace zero
+
+using namespace zero::host;
+
+namespace {
+
+constexpr uint16_t kPoison16 = 0x7FFF;   // a NaN in both fp16 and bf16
+
+int64_t resident_bytes(int scheme, int64_t n, int64_t S) {
+  // bands: 2 (16-bit weight) + 2 (16-bit gradient) + 12 (fp32 master, m, v)
+  const bool so = scheme >= ZERO_SCHEME_Z1, sg = scheme >= ZERO_SCHEME_Z2, sp = scheme >= ZERO_SCHEME_Z3;
+  return 2 * (sp ? S : n) + 2 * (sg ? S : n) + 12 * (so ? S : n);
+}
+
+// Counter slots for bounded device waits: slot 0 belongs to no context, the
+// others are handed to contexts while they live; when all are taken, new
+// contexts share the last one.
+std::mutex g_slot_mu;
+bool g_slot_used[zero::kErrSlots] = {true};
+
+int take_slot() {
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  for (int i = 1; i < zero::kErrSlots; ++i)
+    if (!g_slot_used[i]) {
+      g_slot_used[i] = true;
+      return i;
+    }
+  return zero::kErrSlots - 1;
+}
+
+void give_slot(int i) {
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  if (i > 0 && i < zero::kErrSlots - 1) g_slot_used[i] = false;
 }
 
 int poison_unit(zero_ctx* c, int64_t u, void* buf, cudaStream_t s) {
@@ -448,125 +354,9 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
   return ZERO_OK;
 }
 
-// ---- the step fed from host memory ----------------------------------------------
-
-constexpr int64_t kDefaultChunk = int64_t(1) << 24;
-
-int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
-
-// Elements of the largest chunk (DP/Z1/Z2: the chunk, rounded up to 8;
-// ZeRO-3: the largest padded unit) and the bytes of one rank's slot.
-void staging_geometry(int scheme, int W, const Layout& L, int64_t chunk_elems, int64_t* chunk, int64_t* slot) {
-  if (scheme == ZERO_SCHEME_Z3) {
-    *chunk = L.unit_max;
-  } else {
-    *chunk = round_up(chunk_elems > 0 ? chunk_elems : kDefaultChunk, 8);
-  }
-  *slot = round_up((*chunk + 8) * 2, 256);
-  (void)W;
-}
-
-struct HostJob {
-  int64_t lo, len, unit;   // flat range; unit for ZeRO-3 (else 0)
-};
-
-int run_host_step(zero_ctx* c, const void* const* host_grads, void* host_out, char* staging, int64_t chunk,
-                  int64_t slot, const zero::AdamCoef& coef, cudaStream_t sh, cudaStream_t sd) {
-  int rc = ensure_cuda(c);
-  if (rc) return rc;
-  cudaStream_t su = c->su;
-  const int W = c->W;
-  const bool z3 = c->scheme == ZERO_SCHEME_Z3;
-  std::vector<HostJob> jobs;
-  if (z3) {
-    for (int64_t u = static_cast<int64_t>(c->L.size.size()) - 1; u >= 0; --u)
-      jobs.push_back({c->L.off[u], c->L.shard[u] * W, u});
-  } else {
-    for (int64_t lo = 0; lo < c->L.n_pad; lo += chunk) jobs.push_back({lo, std::min(chunk, c->L.n_pad - lo), 0});
-  }
-  const int64_t J = static_cast<int64_t>(jobs.size());
-  // the staging slots were last read by earlier work on the update stream
-  ZERO_CUDA(cudaEventRecord(c->ev_begin, su));
-  if (sh != su) ZERO_CUDA(cudaStreamWaitEvent(sh, c->ev_begin, 0));
-  if (sd != su) ZERO_CUDA(cudaStreamWaitEvent(sd, c->ev_begin, 0));
-  auto slot_base = [&](int64_t k, int w) { return staging + ((k & 1) * W + w) * slot; };
-  auto h2d = [&](int64_t k) -> int {
-    const HostJob& j = jobs[k];
-    if (k >= 2) ZERO_CUDA(cudaStreamWaitEvent(sh, c->ev_slot_free[k & 1], 0));
-    const int64_t slack = j.lo & 7;
-    for (int w = 0; w < W && j.len > 0; ++w)
-      ZERO_CUDA(cudaMemcpyAsync(slot_base(k, w) + slack * 2, static_cast<const char*>(host_grads[w]) + j.lo * 2,
-                                static_cast<size_t>(j.len) * 2, cudaMemcpyHostToDevice, sh));
-    ZERO_CUDA(cudaEventRecord(c->ev_landed[k & 1], sh));
-    return ZERO_OK;
-  };
-  for (int64_t k = 0; k < std::min<int64_t>(2, J); ++k)
-    if ((rc = h2d(k))) return rc;
-  touch(c, sh);
-  touch(c, sd);
-
-  // ZeRO-3: the forward gathers need no gradients and run while they arrive
-  int64_t seq = 0, held[2] = {0, 0};
-  if (z3) {
-    for (size_t u = 0; u < c->L.size.size(); ++u) {
-      const int b = static_cast<int>(seq++ & 1);
-      c->live_elems -= held[b];
-      held[b] = c->L.shard[u] * W;
-      live_add(c, held[b]);
-      count_gather(c, static_cast<int64_t>(u));
-      if ((rc = launch_gather(c, static_cast<int64_t>(u), c->ubuf[b], su))) return rc;
-    }
-  }
-  for (int64_t k = 0; k < J; ++k) {
-    const HostJob& j = jobs[k];
-    ZERO_CUDA(cudaStreamWaitEvent(su, c->ev_landed[k & 1], 0));
-    const void* g[zero::kMaxRanks];
-    for (int w = 0; w < W; ++w) g[w] = slot_base(k, w) + (j.lo & 7) * 2 - j.lo * 2;
-    if (z3) {
-      const int b = static_cast<int>(seq++ & 1);
-      c->live_elems -= held[b];
-      held[b] = c->L.shard[j.unit] * W;
-      live_add(c, held[b]);
-      count_gather(c, j.unit);
-      if ((rc = launch_update(c, j.unit, g, coef, su, c->ubuf[b]))) return rc;
-      count_scatter(c, j.unit);
-    } else {
-      if ((rc = launch_update(c, 0, g, coef, su, nullptr, j.lo, j.len))) return rc;
-    }
-    ZERO_CUDA(cudaEventRecord(c->ev_slot_free[k & 1], su));
-    ZERO_CUDA(cudaEventRecord(c->ev_updated[k & 1], su));
-    if (host_out != nullptr && j.len > 0) {
-      if (sd != su) ZERO_CUDA(cudaStreamWaitEvent(sd, c->ev_updated[k & 1], 0));
-      char* out = static_cast<char*>(host_out);
-      if (z3) {
-        const int64_t S = c->L.shard[j.unit], o16 = c->L.off16[j.unit];
-        for (int r = 0; r < W; ++r)
-          ZERO_CUDA(cudaMemcpyAsync(out + (r * c->L.shard_total + o16) * 2,
-                                    static_cast<const char*>(c->shard16[r]) + o16 * 2, static_cast<size_t>(S) * 2,
-                                    cudaMemcpyDeviceToHost, sd));
-      } else {
-        ZERO_CUDA(cudaMemcpyAsync(out + j.lo * 2, static_cast<const char*>(c->p16) + j.lo * 2,
-                                  static_cast<size_t>(j.len) * 2, cudaMemcpyDeviceToHost, sd));
-      }
-    }
-    if (k + 2 < J && (rc = h2d(k + 2))) return rc;
-  }
-  if (z3) c->live_elems -= held[0] + held[1];
-  else {
-    // the all-reduce of DP, or the reduce-scatter + all-gather of ZeRO-1/2
-    count_scatter(c, 0);
-    c->gathers += 1;
-    c->comm += ring_bytes(c->W, c->L.shard[0]);
-  }
-  // later work on the update stream comes after the read-back too
-  if (sd != su) {
-    ZERO_CUDA(cudaEventRecord(c->ev_out_done, sd));
-    ZERO_CUDA(cudaStreamWaitEvent(su, c->ev_out_done, 0));
-  }
-  return ZERO_OK;
-}
-
 }  // namespace
+
+int zero::record_error(int code, const char* msg) { return fail(code, "%s", msg); }
 
 int zero::check_adam_args(double lr, double beta1, double beta2, double eps, int64_t t) {
   return check_hyper(lr, beta1, beta2, eps, t);
@@ -786,132 +576,6 @@ int zero_step(zero_ctx* c, int scheme, int W, int64_t n, const void* const* grad
     if (rc) return rc;
   }
   c->t = t;
-  return ZERO_OK;
-}
-
-int64_t zero_host_staging_bytes(int scheme, int W, int64_t n_units, const int64_t* unit_sizes, int64_t chunk_elems) {
-  if (!valid_scheme(scheme)) return fail(ZERO_E_ARG, "scheme %d is not one of DP/Z1/Z2/Z3", scheme);
-  if (scheme != ZERO_SCHEME_Z3 && n_units != 1)
-    return fail(ZERO_E_ARG, "data parallel, ZeRO-1 and ZeRO-2 take exactly one unit");
-  if (chunk_elems < 0 || chunk_elems > (int64_t(1) << 40)) return fail(ZERO_E_ARG, "chunk_elems out of range");
-  Layout L;
-  int rc = make_layout(W, n_units, unit_sizes, &L);
-  if (rc) return rc;
-  int64_t chunk = 0, slot = 0;
-  staging_geometry(scheme, W, L, chunk_elems, &chunk, &slot);
-  return 2 * W * slot;
-}
-
-int zero_step_host(zero_ctx* c, int scheme, int W, int64_t n, const void* const* host_grads, void* host_out,
-                   void* staging, int64_t staging_bytes, int64_t chunk_elems, double lr, double beta1, double beta2,
-                   double eps, int64_t t, void* stream_h2d, void* stream_d2h) {
-  if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
-  if (scheme != c->scheme || W != c->W || n != c->L.n)
-    return fail(ZERO_E_ARG, "scheme/W/n (%d/%d/%lld) differ from the context's (%d/%d/%lld)", scheme, W,
-                (long long)n, c->scheme, c->W, (long long)c->L.n);
-  int rc = check_hyper(lr, beta1, beta2, eps, t);
-  if (rc) return rc;
-  if (t != c->t + 1)
-    return fail(ZERO_E_STATE, "step counter %lld does not follow %lld", (long long)t, (long long)c->t);
-  if (chunk_elems < 0 || chunk_elems > (int64_t(1) << 40)) return fail(ZERO_E_ARG, "chunk_elems out of range");
-  if ((rc = check_no_open_bucket_step(c))) return rc;
-  if (host_grads == nullptr) return fail(ZERO_E_ARG, "host_grads is NULL");
-  for (int w = 0; w < W; ++w)
-    if (host_grads[w] == nullptr && c->L.n_pad > 0) return fail(ZERO_E_ARG, "host gradients of rank %d are NULL", w);
-  int64_t chunk = 0, slot = 0;
-  staging_geometry(c->scheme, W, c->L, chunk_elems, &chunk, &slot);
-  const int64_t need = 2 * W * slot;
-  if (c->L.n_pad > 0) {
-    if (staging == nullptr) return fail(ZERO_E_ARG, "staging is NULL");
-    if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0) return fail(ZERO_E_ALIGN, "staging must be 256-byte aligned");
-    if (staging_bytes < need)
-      return fail(ZERO_E_ARG, "staging holds %lld bytes; this configuration needs %lld", (long long)staging_bytes,
-                  (long long)need);
-  }
-  if ((rc = check_ranks_up(c))) return rc;
-  for (size_t u = 0; u < c->live.size(); ++u)
-    if (c->live[u]) return fail(ZERO_E_STATE, "unit %zu is still gathered by the caller", u);
-  const zero::AdamCoef coef = make_coef(lr, beta1, beta2, eps, t, W);
-  cudaStream_t sh = stream_h2d ? static_cast<cudaStream_t>(stream_h2d) : c->su;
-  cudaStream_t sd = stream_d2h ? static_cast<cudaStream_t>(stream_d2h) : c->su;
-  Range range("zero_step_host %lld", static_cast<long long>(t));
-  if (c->L.n_pad > 0) {
-    rc = run_host_step(c, host_grads, host_out, static_cast<char*>(staging), chunk, slot, coef, sh, sd);
-    if (rc) return rc;
-  }
-  c->t = t;
-  return ZERO_OK;
-}
-
-int zero_step_bucket(zero_ctx* c, int64_t lo, int64_t len, const void* const* bucket_grads, double lr,
-                     double beta1, double beta2, double eps, int64_t t, void* stream) {
-  if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
-  if (c->scheme == ZERO_SCHEME_Z3) return fail(ZERO_E_ARG, "ZeRO-3 updates unit by unit: use zero_update_unit");
-  int rc = check_hyper(lr, beta1, beta2, eps, t);
-  if (rc) return rc;
-  if (len <= 0 || lo < 0 || lo > c->L.n_pad - len)
-    return fail(ZERO_E_ARG, "bucket [%lld, %lld) is not inside [0, %lld)", (long long)lo, (long long)(lo + len),
-                (long long)c->L.n_pad);
-  if (lo % 8 != 0) return fail(ZERO_E_ALIGN, "a bucket must start at a multiple of 8 elements (lo=%lld)", (long long)lo);
-  if (bucket_grads == nullptr) return fail(ZERO_E_ARG, "bucket_grads is NULL");
-  for (int w = 0; w < c->W; ++w) {
-    if (bucket_grads[w] == nullptr) return fail(ZERO_E_ARG, "bucket of rank %d is NULL", w);
-    if (!aligned16(bucket_grads[w])) return fail(ZERO_E_ALIGN, "bucket of rank %d is not 16-byte aligned", w);
-  }
-  const bool new_step = t == c->t + 1;
-  if (new_step) {
-    if ((rc = check_no_open_bucket_step(c))) return rc;
-  } else if (!(t == c->t && c->bucket_open)) {
-    return fail(ZERO_E_STATE, "bucket of step %lld: the context is at step %lld%s", (long long)t, (long long)c->t,
-                c->bucket_open ? "" : " and no bucketed step is open");
-  }
-  if (!new_step) {
-    // no overlap with what this step has already covered
-    auto it = c->covered.upper_bound(lo);
-    if (it != c->covered.end() && it->first < lo + len)
-      return fail(ZERO_E_STATE, "bucket [%lld, %lld) overlaps one already applied in step %lld", (long long)lo,
-                  (long long)(lo + len), (long long)t);
-    if (it != c->covered.begin() && std::prev(it)->second > lo)
-      return fail(ZERO_E_STATE, "bucket [%lld, %lld) overlaps one already applied in step %lld", (long long)lo,
-                  (long long)(lo + len), (long long)t);
-  }
-  if ((rc = check_ranks_up(c))) return rc;
-  for (size_t u = 0; u < c->live.size(); ++u)
-    if (c->live[u]) return fail(ZERO_E_STATE, "unit %zu is still gathered by the caller", u);
-  // the kernel indexes gradients by flat position: shift each bucket back by lo
-  const void* g[zero::kMaxRanks];
-  for (int w = 0; w < c->W; ++w) g[w] = static_cast<const char*>(bucket_grads[w]) - lo * 2;
-  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : c->su;
-  rc = launch_update(c, 0, g, make_coef(lr, beta1, beta2, eps, t, c->W), s, nullptr, lo, len);
-  if (rc) return rc;
-  if (new_step) {
-    c->covered.clear();
-    c->covered_elems = 0;
-    c->bucket_open = true;
-    c->t = t;
-  }
-  // record [lo, lo + len), merging with its neighbours
-  int64_t a = lo, b = lo + len;
-  auto it = c->covered.lower_bound(a);
-  if (it != c->covered.begin() && std::prev(it)->second == a) {
-    --it;
-    a = it->first;
-    it = c->covered.erase(it);
-  }
-  if (it != c->covered.end() && it->first == b) {
-    b = it->second;
-    c->covered.erase(it);
-  }
-  c->covered[a] = b;
-  c->covered_elems += len;
-  if (c->covered_elems == c->L.n_pad) {
-    // the whole vector is done: the step's reduce-scatter and all-gather
-    c->bucket_open = false;
-    c->covered.clear();
-    count_scatter(c, 0);
-    c->gathers += 1;
-    c->comm += ring_bytes(c->W, c->L.shard[0]);
-  }
   return ZERO_OK;
 }
 
