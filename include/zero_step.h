@@ -579,6 +579,15 @@ int zero_offload_init(zero_offload** out, int W, int64_t n, int grad_dtype, int 
 int zero_offload_step(zero_offload* ctx, const void* const* grads, double lr, double beta1, double beta2,
                       double eps, int64_t t);
 
+/*
+ * Resume: set the context's step counter to t (>= 0), the number of steps
+ * already applied to the master, m and v it works on.  The fp32 state lives
+ * in the caller's host buffers, so a checkpoint is those three arrays plus t;
+ * to resume, copy them back and call this.  The next zero_offload_step takes
+ * t + 1.  The device working copy is rewritten by that step.
+ */
+int zero_offload_set_step(zero_offload* ctx, int64_t t);
+
 /* Cumulative figures of a context (any pointer may be NULL): the last step
  * counter, seconds of the steps' host phases (from the wait for the first
  * chunk's mean to the last piece's update), bytes copied device->host and

@@ -105,3 +105,41 @@ def test_gpt2_small_sized_offloaded_step():
         assert_f32_close(off.master.numpy()[idx], orc.master, f"t={t} master sample")
     off.close()
     dev.close()
+
+
+def test_offloaded_step_resumes_from_a_checkpoint():
+    """Save master, m, v and t after 3 steps, restore them into a new context,
+    set its step counter, and the next step equals the uninterrupted run."""
+    n, W = 300_001, 4
+    wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=4, name="offload_resume")
+    theta0 = wk.draw_theta0(wl, "cuda")
+    a = zs.ZeroOffload(W, n, wk.BF16, theta0=theta0.cpu(), threads=3)
+    src = wk.GradSource(wl, wk.BF16, "cuda")
+    steps = []
+    for t in range(1, 5):
+        g = a.new_grad_buffers()
+        for b, d in zip(g, src.step(t)):
+            b[:n].copy_(d)
+        steps.append(g)
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    for t in range(1, 4):
+        a.step(steps[t - 1], *hp, t)
+    saved = [x.clone() for x in (a.master, a.m, a.v)]
+    a.step(steps[3], *hp, 4)
+    torch.cuda.synchronize()
+    b = zs.ZeroOffload(W, n, wk.BF16, threads=2)
+    for dst, src_ in zip((b.master, b.m, b.v), saved):
+        dst.copy_(src_)
+    with pytest.raises(zs.ZeroError) as e:
+        b.step(steps[3], *hp, 4)              # a fresh context expects step 1
+    assert e.value.code == zs.ZERO_E_STATE
+    b.set_step(3)
+    b.step(steps[3], *hp, 4)
+    torch.cuda.synchronize()
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+        assert _equal(x, y)
+    assert _equal(a.p16, b.p16)
+    with pytest.raises(zs.ZeroError):
+        b.set_step(-1)
+    a.close()
+    b.close()

@@ -62,6 +62,7 @@ SIGNATURES = {
     "zero_offload_stats": (_I, [_P, _LP, ctypes.POINTER(ctypes.c_double), _LP, _LP, _LP,
                                 ctypes.POINTER(ctypes.c_int)]),
     "zero_offload_destroy": (_I, [_P]),
+    "zero_offload_set_step": (_I, [_P, _L]),
     "zero_adam_host": (_I, [_L, _P, _P, _P, _P, _P, _I, _D, _D, _D, _D, _L, _I, _I]),
     "zero_host_alloc": (_I, [_L, ctypes.POINTER(_P)]),
     "zero_host_free": (_I, [_P]),
@@ -251,6 +252,10 @@ def zero_offload_stats(ctx) -> dict:
                                                           ctypes.byref(launches), ctypes.byref(threads)))
     return {"t": t.value, "host_seconds": secs.value, "d2h_bytes": d2h.value, "h2d_bytes": h2d.value,
             "launches": launches.value, "threads": threads.value}
+
+
+def zero_offload_set_step(ctx, t: int) -> None:
+    _check("zero_offload_set_step", lib().zero_offload_set_step(ctx, t))
 
 
 def zero_offload_destroy(ctx) -> None:
@@ -588,6 +593,10 @@ class ZeroOffload:
 
     def stats(self):
         return zero_offload_stats(self.ctx)
+
+    def set_step(self, t):
+        """Resume at step t: the host master, m and v must hold the state after step t."""
+        zero_offload_set_step(self.ctx, t)
 
     def close(self):
         if getattr(self, "ctx", None):

@@ -436,6 +436,13 @@ extern "C" int zero_offload_step(zero_offload* c, const void* const* grads, doub
   return ZERO_OK;
 }
 
+extern "C" int zero_offload_set_step(zero_offload* c, int64_t t) {
+  if (!c) return fail(ZERO_E_ARG, "context is NULL");
+  if (t < 0) return fail(ZERO_E_ARG, "the step counter cannot be negative");
+  c->t = t;
+  return ZERO_OK;
+}
+
 extern "C" int zero_offload_stats(const zero_offload* c, int64_t* t, double* host_seconds, int64_t* d2h_bytes,
                                   int64_t* h2d_bytes, int64_t* launches, int* threads) {
   if (!c) return fail(ZERO_E_ARG, "context is NULL");
