@@ -18,7 +18,6 @@
 
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -70,10 +69,8 @@ extern "C" int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_s
   if (n_units < 1 || unit_sizes == nullptr) return set_error(ZERO_E_ARG, "need at least one unit");
   if ((grad_dtype != ZERO_FP16 && grad_dtype != ZERO_BF16) || (work_dtype != ZERO_FP16 && work_dtype != ZERO_BF16))
     return set_error(ZERO_E_ARG, "16-bit formats must be ZERO_FP16 or ZERO_BF16");
-  if (!std::isfinite(lr) || lr < 0 || !(beta1 >= 0 && beta1 < 1) || !(beta2 >= 0 && beta2 < 1) ||
-      !std::isfinite(eps) || !(eps > 0))
-    return set_error(ZERO_E_ARG, "Adam hyper-parameters out of range");
-  if (t < 1) return set_error(ZERO_E_STATE, "the step counter starts at 1");
+  int rc = zero::check_adam_args(lr, beta1, beta2, eps, t);
+  if (rc) return rc;
   // the same layout as every ZeRO-3 context: units padded to S_u * W, one
   // after another (walked forward here, and backward for the backward pass)
   int64_t pos = 0, pos16 = 0;
@@ -97,8 +94,7 @@ extern "C" int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_s
       return set_error(ZERO_E_ALIGN, "shard stores and gradients must be 16-byte aligned");
   }
   void* buf = nullptr;
-  int rc = unit_scratch(&buf);
-  if (rc) return rc;
+  if ((rc = unit_scratch(&buf))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   zero::FusedLaunch a{};
@@ -110,11 +106,7 @@ extern "C" int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_s
   a.m = m;
   a.v = v;
   a.variant = ZERO_VARIANT_AUTO;
-  const double bc1 = 1.0 - std::pow(beta1, static_cast<double>(t));
-  const double bc2 = 1.0 - std::pow(beta2, static_cast<double>(t));
-  a.coef = {static_cast<float>(beta1), static_cast<float>(1.0 - beta1), static_cast<float>(beta2),
-            static_cast<float>(1.0 - beta2), static_cast<float>(lr / bc1), static_cast<float>(1.0 / std::sqrt(bc2)),
-            static_cast<float>(eps), static_cast<float>(1.0 / W)};
+  a.coef = zero::adam_coef(lr, beta1, beta2, eps, t, W);
   int64_t launches = 0;
   // One stream and one buffer: each gather waits, in stream order, for the
   // work that used the previous unit.
