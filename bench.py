@@ -470,14 +470,16 @@ def run_ours(args):
     if not args.no_e2e and args.e2e_steps > 0:
         # host buffers from zero_host_alloc: page-locked on huge pages, where the
         # link holds its full rate (memory from cudaHostAlloc measured slower)
-        host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in step.grads]
+        # one block for the W gradient vectors and the read-back (all 16-bit),
+        # so that even vectors smaller than a huge page sit on huge pages
         out_elems = step.n_pad if scheme != 3 else wl.W * step.sizes["shard_store"]
-        host_bufs.append(zs.HostBuffer(out_elems, step.work_torch_dtype))
+        host_bufs = [zs.HostBuffer(wl.W * step.n_pad + out_elems, torch.int16)]
         huge_at_alloc = huge_page_fraction(host_bufs)
-        host_grads = [b.tensor for b in host_bufs[:-1]]
+        block = host_bufs[0].tensor
+        host_grads = [block[r * step.n_pad:(r + 1) * step.n_pad].view(step.grad_torch_dtype) for r in range(wl.W)]
+        host_out = block[wl.W * step.n_pad:].view(step.work_torch_dtype)
         for h, g in zip(host_grads, step.grads):
             h.copy_(g)
-        host_out = host_bufs[-1].tensor
         need = zs.zero_host_staging_bytes(scheme, wl.W, units, 0)
         staging = torch.empty(need, dtype=torch.uint8, device=dev)
         sh, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -512,7 +514,7 @@ def run_ours(args):
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "staging_bytes": need,
                "path": "zero_step_host: host gradients (zero_host_alloc) -> 2-slot device staging ring -> "
                        "fused step -> 16-bit working copy -> host, pipelined over three streams", "link": link}
-        del host_grads, host_out, staging
+        del host_grads, host_out, staging, block
         for b in host_bufs:
             b.close()
 
@@ -592,6 +594,59 @@ def gpu_uuid(dev):
     return f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or dev.index)
 
 
+def e2e_through_torch_copies(args, world, wl, su, grads, result, run_step, t0, path):
+    """End to end for the entry points that take device gradients: every
+    step copies the W gradient vectors in from page-locked host memory
+    (zero_host_alloc), runs the step, and reads ``result`` (a device tensor)
+    back to host memory, all in order on ``su``.  ``run_step(t)`` enqueues one
+    step.  Returns (the e2e dict, the last step counter used)."""
+    import torch
+    import torch.distributed as dist
+    import zero_sharded_mixed_step_gb300 as zs
+    # one block for the W gradient vectors and the read-back (all 16-bit), so
+    # that even vectors smaller than a huge page sit on huge pages
+    n, W = grads[0].numel(), len(grads)
+    host_bufs = [zs.HostBuffer(W * n + result.numel(), torch.int16)]
+    huge_at_alloc = huge_page_fraction(host_bufs)
+    block = host_bufs[0].tensor
+    host_grads = [block[r * n:(r + 1) * n].view(grads[0].dtype) for r in range(W)]
+    host_out = block[W * n:].view(result.dtype)
+    for h, g in zip(host_grads, grads):
+        h.copy_(g)
+    t = t0
+
+    def host_step():
+        nonlocal t
+        t += 1
+        with torch.cuda.stream(su):
+            for g, h in zip(grads, host_grads):
+                g.copy_(h, non_blocking=True)
+            run_step(t)
+            host_out.copy_(result, non_blocking=True)
+
+    link = link_probe(list(zip(grads, host_grads)), [(host_out, result)], su)
+    link["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
+    link["host_huge_page_fraction_at_alloc"] = huge_at_alloc
+    for _ in range(2):               # warm the path, untimed
+        host_step()
+    su.synchronize()
+    if world > 1:
+        dist.barrier()
+    h0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        host_step()
+    su.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - h0)
+    e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
+           "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
+           "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
+           "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "path": path, "link": link}
+    del host_grads, host_out, block
+    for b in host_bufs:
+        b.close()
+    return e2e, t
+
+
 def run_replicas(args, wl, dtype, world, rank, dev):
     """Plain data parallelism with the W replicas kept literally
     (zero_step_dp_replicas): every rank's fp32 master, m, v and 16-bit copy
@@ -651,48 +706,12 @@ def run_replicas(args, wl, dtype, world, rank, dev):
                 "launch_ms": ms_per_step, "algorithmic_bytes_per_launch": step_bytes,
                 "bytes_per_element": per_elem, "frac_of_8tbs_nominal": achieved / 8000.0, "launches_timed": launches}
 
-    # end to end: every step copies the W gradient vectors in from page-locked
-    # host memory (zero_host_alloc) and reads replica 0's 16-bit working copy back
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
-        host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in grads]
-        host_grads = [b.tensor for b in host_bufs]
-        for h, g in zip(host_grads, grads):
-            h.copy_(g)
-        host_bufs.append(zs.HostBuffer(rep.n_pad, rep.work_torch_dtype))
-        host_out = host_bufs[-1].tensor
-
-        def host_step():
-            nonlocal t
-            t += 1
-            with torch.cuda.stream(su):
-                for g, h in zip(grads, host_grads):
-                    g.copy_(h, non_blocking=True)
-                rep.step(grads, *hp, t)
-                host_out.copy_(rep.p16[0], non_blocking=True)
-
-        link = link_probe(list(zip(grads, host_grads)), [(host_out, rep.p16[0])], su)
-        link["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
-        for _ in range(2):               # warm the path, untimed
-            host_step()
-        su.synchronize()
-        if world > 1:
-            dist.barrier()
-        h0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            host_step()
-        su.synchronize()
-        e2e_s = max_over_ranks(time.perf_counter() - h0)
-        e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
-               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
-               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
-               "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
-               "path": "host gradients (zero_host_alloc) -> device gradient buffers (one copy per rank) -> "
-                       "zero_step_dp_replicas -> replica 0's 16-bit working copy -> host, one stream",
-               "link": link}
-        del host_grads, host_out
-        for b in host_bufs:
-            b.close()
+        e2e, t = e2e_through_torch_copies(
+            args, world, wl, su, grads, rep.p16[0], lambda tt: rep.step(grads, *hp, tt), t,
+            "host gradients (zero_host_alloc) -> device gradient buffers (one copy per rank) -> "
+            "zero_step_dp_replicas -> replica 0's 16-bit working copy -> host, one stream")
 
     resident = sum(x.numel() * x.element_size() for x in rep.master + rep.m + rep.v + rep.p16)
     del rep, grads
@@ -796,42 +815,10 @@ def run_offload(args, wl, dtype, world, rank, dev):
 
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
-        host_bufs = [zs.HostBuffer(g.numel(), g.dtype) for g in grads]
-        host_grads = [b.tensor for b in host_bufs]
-        for h, g in zip(host_grads, grads):
-            h.copy_(g)
-        host_bufs.append(zs.HostBuffer(off.n_pad, off.work_torch_dtype))
-        host_out = host_bufs[-1].tensor
-
-        def host_step():
-            nonlocal t
-            t += 1
-            with torch.cuda.stream(su):
-                for g, h in zip(grads, host_grads):
-                    g.copy_(h, non_blocking=True)
-                off.step(grads, *hp, t)
-                host_out.copy_(off.p16, non_blocking=True)
-
-        probe = link_probe(list(zip(grads, host_grads)), [(host_out, off.p16)], su)
-        probe["host_huge_page_fraction"] = huge_page_fraction(host_bufs)
-        for _ in range(2):
-            host_step()
-        su.synchronize()
-        h0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            host_step()
-        su.synchronize()
-        e2e_s = max_over_ranks(time.perf_counter() - h0)
-        e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
-               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
-               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
-               "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
-               "path": "host gradients (zero_host_alloc) -> device gradient buffers -> zero_offload_step "
-                       "(device mean, host Adam, 16-bit copy back) -> 16-bit working copy -> host",
-               "link": probe}
-        del host_grads, host_out
-        for b in host_bufs:
-            b.close()
+        e2e, t = e2e_through_torch_copies(
+            args, world, wl, su, grads, off.p16, lambda tt: off.step(grads, *hp, tt), t,
+            "host gradients (zero_host_alloc) -> device gradient buffers -> zero_offload_step "
+            "(device mean, host Adam, 16-bit copy back) -> 16-bit working copy -> host")
 
     off.close()
     del grads
