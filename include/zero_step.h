@@ -306,7 +306,9 @@ int zero_step_host(zero_ctx* ctx, int scheme, int W, int64_t n, const void* cons
  * mapped as whole huge pages from a huge-page boundary (its last page may
  * extend past `bytes`); a smaller one starts on a page boundary, on base
  * pages.
- * The contents are zero.  *out receives the address (NULL on
+ * The contents are zero.  For many vectors (e.g. every rank's gradients)
+ * one block, sliced, keeps them all on huge pages even when each is
+ * smaller than a huge page.  *out receives the address (NULL on
  * failure).  The memory is the caller's until zero_host_free.
  * ZERO_E_ARG for bytes <= 0 or out NULL; ZERO_E_NOMEM if the mapping
  * fails; ZERO_E_CUDA if the registration fails (e.g. no device).
