@@ -5,8 +5,8 @@
 // base pages; on GB300 hosts its 1 GB copies measured anywhere from 38 to
 // 212 GB/s, with more slow stretches in each later process on the same host,
 // while memory mapped here (anonymous, advised for huge pages, populated,
-// then registered) held 208-212 GB/s in every run.  The address translation
-// of DMA over many small pages is the likely cost.
+// then registered) held 208-212 GB/s in the same processes.  The address
+// translation of DMA over many small pages is the likely cost.
 
 #include <sys/mman.h>
 #include <unistd.h>
