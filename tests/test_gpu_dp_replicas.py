@@ -63,6 +63,7 @@ RAGGED = [
     (65_537, 16, wk.FP16, wk.BF16),
     (7, 1, wk.BF16, wk.FP16),
     (333_333, 5, wk.BF16, wk.BF16),
+    (10_001, 64, wk.FP16, wk.FP16),         # the most ranks a context takes
 ]
 
 

@@ -20,6 +20,7 @@ CASES = [
     (2_000_000, 16, wk.FP16, wk.BF16, 0),
     (7, 1, wk.BF16, wk.FP16, 8),
     (250_001, 5, wk.BF16, wk.BF16, 100),
+    (20_000, 64, wk.FP16, wk.FP16, 1000),   # the most ranks a context takes
 ]
 
 
