@@ -229,11 +229,13 @@ def check_host_memory(need: int, what: str) -> None:
         raise MemoryError(f"{what} needs about {need / 1e9:.1f} GB of host memory; {avail / 1e9:.1f} GB available")
 
 
-def oracle_sample_step_seconds(wl, sample_elems: int, dtype: str):
-    """Seconds the oracle takes for one step of ``wl`` restricted to a sample
-    of about ``sample_elems`` parameters (ZeRO-3: whole units shrunk to that
-    size; otherwise the first sample_elems parameters), on synthetic draws."""
-    import numpy as np
+def oracle_sample_steps(wl, sample_elems: int, dtype: str, budget_s: float = 0.0, max_steps: int = 1):
+    """The oracle on a sample of about ``sample_elems`` parameters of ``wl``
+    (ZeRO-3: one unit shrunk to that size; otherwise the first sample_elems
+    parameters), on synthetic draws: steps t = 1, 2, ... until ``budget_s``
+    seconds of oracle time are spent or ``max_steps`` steps are done (at
+    least one).  Returns (seconds in the oracle's steps, parameters of the
+    sample, steps run); drawing the inputs is not timed."""
     import workloads as wk
     from oracle import zero_oracle as z
     scheme = scheme_of(wl)
@@ -244,13 +246,23 @@ def oracle_sample_step_seconds(wl, sample_elems: int, dtype: str):
     small = wk.scaled(wl, unit_sizes=units, name=wl.name + "_sample") if scheme == 3 else \
         wk.scaled(wl, n=sample_elems, name=wl.name + "_sample")
     theta0 = wk.draw_theta0(small, "cpu").numpy()
-    draws = [wk.to_numpy16(g) for g in wk.GradSource(small, dtype, "cpu").step(1)]
     orc = z.make_scheme(scheme, W, theta0, dtype, units if scheme == 3 else None)
-    grads = [z.place(g, orc.layout) for g in draws]
-    t0 = time.perf_counter()
-    orc.step(grads, wl.lr, wl.beta1, wl.beta2, wl.eps)
-    dt = time.perf_counter() - t0
-    return dt, small.n
+    src = wk.GradSource(small, dtype, "cpu")
+    total, steps = 0.0, 0
+    while steps < max(1, max_steps) and (steps == 0 or total < budget_s):
+        grads = [z.place(wk.to_numpy16(g), orc.layout) for g in src.step(steps + 1)]
+        t0 = time.perf_counter()
+        orc.step(grads, wl.lr, wl.beta1, wl.beta2, wl.eps)
+        total += time.perf_counter() - t0
+        steps += 1
+        del grads
+    return total, small.n, steps
+
+
+def oracle_sample_step_seconds(wl, sample_elems: int, dtype: str):
+    """Seconds of one oracle step (t = 1) on a sample (see oracle_sample_steps)."""
+    dt, n, _ = oracle_sample_steps(wl, sample_elems, dtype)
+    return dt, n
 
 
 def cpu_cores_note():
@@ -276,15 +288,19 @@ def calibrate_sample(wl, dtype, budget_s):
 
 
 def cpu_baseline(wl, dtype, budget_s):
+    """The oracle as it stands, timed on this host for about ``budget_s``
+    seconds: a sample sized so that one step takes about that long (capped
+    at the workload, or at one unit for ZeRO-3), run for as many steps as
+    the budget holds (at most 20)."""
     size = calibrate_sample(wl, dtype, budget_s)
-    dt, n = oracle_sample_step_seconds(wl, size, dtype)
+    dt, n, steps = oracle_sample_steps(wl, size, dtype, budget_s, max_steps=20)
     host_cores, model = cpu_cores_note()
-    what = (f"one step (t=1) of the oracle on {n:,} of the {wl.n:,} parameters "
+    what = (f"{steps} step(s) (t = 1..{steps}) of the oracle on {n:,} of the {wl.n:,} parameters "
             + ("(one unit shrunk to that size, full ZeRO-3 schedule)" if scheme_of(wl) == 3 else "(leading slice)")
             + f", W={wl.W}, {dtype} gradients; NumPy elementwise, one thread of {host_cores} host cores"
             + (f" ({model})" if model else ""))
-    return {"value": n / dt, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": what,
-            "seconds": round(dt, 3)}
+    return {"value": n * steps / dt, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": what,
+            "seconds": round(dt, 3), "steps": steps}
 
 
 def run_reference(args):
