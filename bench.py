@@ -348,7 +348,9 @@ def config_of(wl, dtype, gpus):
                   f"{L2_BYTES / 2**20:.0f} MiB of L2",
             "parallelism": "simulated DP ranks in one GPU" + (f"; {gpus} independent replicas" if gpus > 1 else ""),
             "zero3_schedule": ("per unit: forward gather; backward gather fused into the update pass; one stream "
-                               "(no unit hook registered)") if scheme_of(wl) == 3 else None}
+                               "(no unit hook registered); the step's launches replayed from a CUDA graph "
+                               "(zero_set_graph), the per-launch timing pass as ordinary launches")
+            if scheme_of(wl) == 3 else None}
 
 
 # ---- several GPUs: independent replicas -----------------------------------------------
@@ -404,6 +406,8 @@ def run_ours(args):
         theta0 = wk.draw_theta0(wl, dev)
         step = zs.ZeroStep(scheme, wl.W, units, dtype, theta0=theta0, device=dev, stream=su, gather_stream=sg,
                            with_grad_buffers=True)
+        if scheme == 3:
+            step.set_graph(True)     # the step's 2 U launches replayed from one captured graph
         del theta0
         for r, d in enumerate(wk.GradSource(wl, dtype, dev).step(1)):
             step.place_(step.grads[r], d)

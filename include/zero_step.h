@@ -408,13 +408,29 @@ int zero_set_debug(zero_ctx* ctx, int flags);
 
 /*
  * Select the fused-pass variant (ZERO_VARIANT_*).  AUTO uses the bulk-staged
- * kernel where it measured faster (W of 8 or 16, at least one 2048-element
- * tile) and the vector kernel elsewhere.  BULK asks for the bulk-staged
- * kernel; it still runs the vector kernel where the bulk one cannot (W not
- * in {1, 2, 4, 8, 16}, or 16-bit slots not 16-byte aligned).  Both give
- * bit-identical results.
+ * kernel where it measured no slower (W of 8 or 16, at least 8 2048-element
+ * tiles for each CTA) and the vector kernel elsewhere.  BULK asks for the
+ * bulk-staged kernel; it still runs the vector kernel where the bulk one
+ * cannot (W not in {1, 2, 4, 8, 16}, or 16-bit slots not 16-byte aligned).
+ * Both give bit-identical results.  Changing the variant drops a captured
+ * step graph (zero_set_graph).
  */
 int zero_set_variant(zero_ctx* ctx, int variant);
+
+/*
+ * ZeRO-3 steps from a CUDA graph (on != 0) or as ordinary launches (0, the
+ * default).  With it on, the first zero_step that runs without a unit hook,
+ * timing brackets, debug flags or an injected stall captures its 2 U
+ * launches into a graph; that step and every later one with the same
+ * conditions set the fused kernels' Adam coefficients and gradient pointers
+ * on the graph and launch it once on the update stream, which saves the gaps
+ * between the launches.  Steps under other conditions run the ordinary
+ * launches; results are bit-identical either way and the counters advance
+ * the same.  ZERO_E_ARG for a scheme other than ZeRO-3 (one launch per step:
+ * nothing to capture) or a context whose update stream is the legacy default
+ * stream (it cannot be captured).  Turning it off frees the graph.
+ */
+int zero_set_graph(zero_ctx* ctx, int on);
 
 /*
  * Testing the bounded device waits.  The next fused launch of this context,

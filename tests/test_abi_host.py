@@ -291,3 +291,13 @@ def test_host_alloc_checks(zlib):
     assert _err(zs.zero_host_free, 0x1000) == zs.ZERO_E_ARG
     assert "zero_host_alloc" in zs.zero_last_error()
     zs.zero_host_free(None)
+
+
+def test_graph_mode_checks(zlib):
+    """Graph capture is for ZeRO-3 contexts on a created stream only."""
+    z1 = make_ctx(scheme=1)
+    assert _err(zs.zero_set_graph, z1, True) == zs.ZERO_E_ARG
+    zs.zero_set_graph(z1, False)                 # turning it off is always fine
+    z3 = make_ctx(scheme=3, W=4, units=(37, 5))
+    assert _err(zs.zero_set_graph, z3, True) == zs.ZERO_E_ARG   # no stream: the legacy default stream
+    assert "legacy" in zs.zero_last_error()

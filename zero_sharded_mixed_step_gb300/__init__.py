@@ -77,6 +77,7 @@ SIGNATURES = {
     "zero_enable_timing": (_I, [_P, _I]),
     "zero_read_timing": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _LP]),
     "zero_set_variant": (_I, [_P, _I]),
+    "zero_set_graph": (_I, [_P, _I]),
     "zero_inject_stall": (_I, [_P, _L]),
     "zero_set_debug": (_I, [_P, _I]),
     "zero_mark_rank": (_I, [_P, _I, _I]),
@@ -352,6 +353,10 @@ def zero_set_variant(ctx, variant: int) -> None:
     _check("zero_set_variant", lib().zero_set_variant(ctx, variant))
 
 
+def zero_set_graph(ctx, on: bool) -> None:
+    _check("zero_set_graph", lib().zero_set_graph(ctx, 1 if on else 0))
+
+
 def zero_set_debug(ctx, flags: int) -> None:
     _check("zero_set_debug", lib().zero_set_debug(ctx, flags))
 
@@ -478,6 +483,9 @@ class ZeroStep:
 
     def set_variant(self, variant):
         zero_set_variant(self.ctx, variant)
+
+    def set_graph(self, on=True):
+        zero_set_graph(self.ctx, on)
 
     def set_debug(self, flags):
         zero_set_debug(self.ctx, flags)

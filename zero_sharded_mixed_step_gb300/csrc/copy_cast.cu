@@ -117,6 +117,8 @@ cudaError_t launch_fill16(void* dst, int64_t count, uint16_t value, cudaStream_t
   return cudaGetLastError();
 }
 
+const void* copy_kernel() { return reinterpret_cast<const void*>(copy_segments); }
+
 cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int64_t* launches) {
   if (nseg <= 0) return cudaSuccess;
   if (nseg > kMaxCopySegs) return cudaErrorInvalidValue;

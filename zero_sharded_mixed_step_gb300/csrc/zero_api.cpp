@@ -354,6 +354,109 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
   return ZERO_OK;
 }
 
+// ---- ZeRO-3 steps replayed from a CUDA graph ----------------------------------------
+//
+// A ZeRO-3 step without a hook is a fixed sequence of 2 U launches on one
+// stream.  Captured once, it is replayed as one graph launch, which saves the
+// launch gaps between its kernels; only the fused kernels' Adam coefficients
+// and gradient pointers change from step to step, and they are set on the
+// graph's nodes before each replay.
+
+void drop_graph(zero_ctx* c) {
+  if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+  if (c->graph) cudaGraphDestroy(c->graph);
+  c->graph_exec = nullptr;
+  c->graph = nullptr;
+  c->graph_fused.clear();
+}
+
+// Whether this step may run from the graph: anything that adds or changes
+// work (a hook, timing brackets, poisoning, an injected stall) runs the
+// ordinary launches instead.
+bool graph_applies(const zero_ctx* c) {
+  return c->graph_on && c->scheme == ZERO_SCHEME_Z3 && c->hook == nullptr && !c->timing && c->debug == 0 &&
+         !c->stall_pending;
+}
+
+// Capture one step's launches into c->graph (nothing runs) and remember what
+// the step adds to the counters.
+int capture_zero3(zero_ctx* c, const void* const* grads, const zero::AdamCoef& coef) {
+  int rc = ensure_cuda(c);
+  if (rc) return rc;
+  if (!c->err_slot_ready) {   // the counter reset stays outside the graph
+    const cudaError_t e0 = zero::reset_device_errors(c->err_slot, c->su);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "clearing the device error counter");
+    c->err_slot_ready = true;
+  }
+  const int64_t comm = c->comm, launches = c->launches, gathers = c->gathers, scatters = c->scatters;
+  ZERO_CUDA(cudaStreamBeginCapture(c->su, cudaStreamCaptureModeThreadLocal));
+  rc = run_zero3_step(c, grads, coef);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(c->su, &g);
+  c->graph_comm = c->comm - comm;
+  c->graph_launches = c->launches - launches;
+  c->graph_gathers = c->gathers - gathers;
+  c->graph_scatters = c->scatters - scatters;
+  c->comm = comm;               // the captured work has not run yet
+  c->launches = launches;
+  c->gathers = gathers;
+  c->scatters = scatters;
+  if (rc || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return rc ? rc : cuda_fail(e, "capturing the ZeRO-3 step");
+  }
+  c->graph = g;
+  size_t count = 0;
+  cudaError_t e1 = cudaGraphGetNodes(g, nullptr, &count);
+  std::vector<cudaGraphNode_t> nodes(count);
+  if (e1 == cudaSuccess && count) e1 = cudaGraphGetNodes(g, nodes.data(), &count);
+  for (size_t k = 0; e1 == cudaSuccess && k < count; ++k) {
+    cudaGraphNodeType type;
+    e1 = cudaGraphNodeGetType(nodes[k], &type);
+    if (e1 != cudaSuccess || type != cudaGraphNodeTypeKernel) continue;
+    cudaKernelNodeParams p;
+    e1 = cudaGraphKernelNodeGetParams(nodes[k], &p);
+    if (e1 == cudaSuccess && p.func != zero::copy_kernel())
+      c->graph_fused.emplace_back(nodes[k], *static_cast<const zero::FusedLaunch*>(p.kernelParams[0]));
+  }
+  if (e1 == cudaSuccess) e1 = cudaGraphInstantiate(&c->graph_exec, g, 0);
+  if (e1 != cudaSuccess) {
+    drop_graph(c);
+    return cuda_fail(e1, "building the ZeRO-3 step graph");
+  }
+  int64_t updates = 0;
+  for (int64_t u = 0; u < static_cast<int64_t>(c->L.size.size()); ++u) updates += c->L.shard[u] > 0;
+  if (static_cast<int64_t>(c->graph_fused.size()) != updates) {
+    drop_graph(c);
+    return fail(ZERO_E_CUDA, "the captured ZeRO-3 step has %zu update launches, expected %lld",
+                c->graph_fused.size(), static_cast<long long>(updates));
+  }
+  return ZERO_OK;
+}
+
+// One step from the graph: this step's coefficients and gradients on the
+// fused nodes, then one graph launch on the update stream.
+int replay_zero3(zero_ctx* c, const void* const* grads, const zero::AdamCoef& coef) {
+  for (auto& node : c->graph_fused) {
+    zero::FusedLaunch a = node.second;
+    a.coef = coef;
+    for (int w = 0; w < c->W; ++w) a.grads[w] = grads[w];
+    cudaKernelNodeParams p;
+    ZERO_CUDA(cudaGraphKernelNodeGetParams(node.first, &p));
+    void* args[] = {&a};
+    p.kernelParams = args;
+    p.extra = nullptr;
+    ZERO_CUDA(cudaGraphExecKernelNodeSetParams(c->graph_exec, node.first, &p));
+  }
+  ZERO_CUDA(cudaGraphLaunch(c->graph_exec, c->su));
+  c->comm += c->graph_comm;
+  c->launches += c->graph_launches;
+  c->gathers += c->graph_gathers;
+  c->scatters += c->graph_scatters;
+  touch(c, c->su);
+  return ZERO_OK;
+}
+
 }  // namespace
 
 int zero::record_error(int code, const char* msg) { return fail(code, "%s", msg); }
@@ -502,6 +605,7 @@ int zero_destroy(zero_ctx* c) {
       cudaEventDestroy(pr.second);
     }
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+  drop_graph(c);
   give_slot(c->err_slot);
   if (c->cuda_ready) {
     cudaEventDestroy(c->ev_begin);
@@ -571,6 +675,9 @@ int zero_step(zero_ctx* c, int scheme, int W, int64_t n, const void* const* grad
     count_scatter(c, 0);
     c->gathers += 1;
     c->comm += ring_bytes(c->W, c->L.shard[0]);
+  } else if (graph_applies(c)) {
+    if (!c->graph_exec && (rc = capture_zero3(c, grads, coef))) return rc;
+    if ((rc = replay_zero3(c, grads, coef))) return rc;
   } else {
     rc = run_zero3_step(c, grads, coef);
     if (rc) return rc;
@@ -777,7 +884,19 @@ int zero_set_variant(zero_ctx* c, int variant) {
   if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
   if (variant != ZERO_VARIANT_AUTO && variant != ZERO_VARIANT_VECTOR && variant != ZERO_VARIANT_BULK)
     return fail(ZERO_E_ARG, "unknown variant %d", variant);
+  if (variant != c->variant) drop_graph(c);   // the captured launches used the old choice
   c->variant = variant;
+  return ZERO_OK;
+}
+
+int zero_set_graph(zero_ctx* c, int on) {
+  if (c == nullptr) return fail(ZERO_E_ARG, "ctx is NULL");
+  if (on && c->scheme != ZERO_SCHEME_Z3)
+    return fail(ZERO_E_ARG, "only ZeRO-3 steps launch more than one kernel; there is nothing to capture");
+  if (on && c->su == nullptr)
+    return fail(ZERO_E_ARG, "graph capture needs a created update stream, not the legacy default stream");
+  c->graph_on = on != 0;
+  if (!c->graph_on) drop_graph(c);
   return ZERO_OK;
 }
 

@@ -108,6 +108,14 @@ struct zero_ctx {
   int64_t covered_elems = 0;
   std::vector<cudaEvent_t> event_pool;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed[3];
+  // ZeRO-3 steps replayed from a CUDA graph (zero_set_graph): the captured
+  // step, its fused-kernel nodes with their launch arguments, and what one
+  // step adds to the counters
+  bool graph_on = false;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  std::vector<std::pair<cudaGraphNode_t, zero::FusedLaunch>> graph_fused;
+  int64_t graph_comm = 0, graph_launches = 0, graph_gathers = 0, graph_scatters = 0, graph_peak = 0;
 };
 
 namespace zero {

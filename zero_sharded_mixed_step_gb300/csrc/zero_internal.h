@@ -88,6 +88,9 @@ cudaError_t launch_fused_step(const FusedLaunch& a, cudaStream_t stream, int64_t
 // Gather: copy each segment's bytes (16-byte vectors where both ends allow).
 cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int64_t* launches);
 
+// The gather kernel's device function (to tell its nodes apart in a captured graph).
+const void* copy_kernel();
+
 // Fill count 16-bit values with `value` (debug poisoning of released units).
 cudaError_t launch_fill16(void* dst, int64_t count, uint16_t value, cudaStream_t stream, int64_t* launches);
 
