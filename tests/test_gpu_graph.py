@@ -125,3 +125,35 @@ def test_graph_steps_against_the_oracle():
             run.compare()
         assert run.padding_is_zero()
         run.close()
+
+
+def test_full_zero3_workload_as_the_benchmark_runs_it():
+    """The 24 x 50,331,648 workload on 8 ranks without a hook and with graph
+    replay, the launch configuration the benchmark times: sampled parity with
+    the oracle, bit-identical to ordinary launches on the same gradients,
+    traffic 6,341,787,648 B and 2 U launches per step, two unit buffers at
+    most."""
+    wl = wk.scaled(wk.LAYER_UNITS, steps=3)
+    U, S_u = len(wl.units()), wl.units()[0] // wl.W
+    sample = gh.sample_real_indices(wl.n, wl.W, wl.units(), k=16384)
+    with torch.cuda.stream(_stream()):
+        run = gh.Run(wl, zs.ZERO_SCHEME_Z3, "bf16", sample=sample, gather_stream=False)
+        run.zs.set_graph(True)
+        plain = zs.ZeroStep(zs.ZERO_SCHEME_Z3, wl.W, wl.units(), "bf16",
+                            theta0=wk.draw_theta0(wl, "cuda"), stream=_stream())
+        launches0 = run.zs.stat(zs.ZERO_STAT_LAUNCHES)
+        for _ in range(wl.steps):
+            run.step()
+            plain.step(run.zs.grads, wl.lr, wl.beta1, wl.beta2, wl.eps, run.t)
+        torch.cuda.synchronize()
+        run.compare()
+        for x, y in ((run.zs.master, plain.master), (run.zs.m, plain.m), (run.zs.v, plain.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+        for a, b in zip(run.zs.shard16, plain.shard16):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert zs.zero_comm_bytes_per_rank(run.zs.ctx) == wl.steps * 6_341_787_648
+        assert run.zs.stat(zs.ZERO_STAT_LAUNCHES) - launches0 == wl.steps * 2 * U
+        assert run.zs.stat(zs.ZERO_STAT_PEAK_LIVE_ELEMS) == 2 * S_u * wl.W
+        assert run.zs.stat(zs.ZERO_STAT_LIVE_ELEMS) == 0
+        plain.close()
+        run.close()
