@@ -23,6 +23,16 @@
  *     4.1.4 and appendix B, "Sharding the States": traffic per rank under
  *     ring collectives, (N-1)/N of the data per collective.
  *
+ * Beside the step itself (zero_step, and zero_gather_unit / zero_update_unit
+ * / zero_release_unit for callers that drive ZeRO-3 themselves) the library
+ * offers: the step fed from host memory (zero_step_host) with its host
+ * allocator (zero_host_alloc); the step applied bucket by bucket
+ * (zero_step_bucket); ZeRO-3 steps replayed from a CUDA graph
+ * (zero_set_graph); a ZeRO-3 step that allocates nothing
+ * (zero_step_z3_static); data parallelism with its replicas kept literally
+ * (zero_step_dp_replicas); and ZeRO-2 with the optimizer on the host CPU
+ * (zero_offload_*).
+ *
  * Layout.  n real parameters are split into units (one unit for data
  * parallel, ZeRO-1 and ZeRO-2; the caller's units, e.g. one per transformer
  * layer, for ZeRO-3).  Unit u holds unit_sizes[u] parameters padded with
