@@ -477,8 +477,10 @@ def run_ours(args):
                 "launches_timed": fused_n, "timing_pass_ms_per_step": ms_instr / args.steps}
     gather_info = None
     if gather_n:
-        gb = 4 * per_launch[0]
-        gather_info = {"launch_ms": gather_ms / gather_n, "achieved_gbs": gb / (gather_ms / gather_n / 1e3) / 1e9,
+        # the forward gathers move 2 bytes in and 2 out per element of every unit,
+        # two units per launch (the backward gathers are inside the fused pass)
+        gather_bytes = 4 * n_pad * args.steps
+        gather_info = {"launch_ms": gather_ms / gather_n, "achieved_gbs": gather_bytes / (gather_ms / 1e3) / 1e9,
                        "launches": gather_n, "share_of_bracketed_time": gather_ms / (gather_ms + fused_ms)}
 
     # ---- end to end: gradients from page-locked host memory, working copy read back --

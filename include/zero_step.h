@@ -224,7 +224,8 @@ int zero_refresh_working_copy(zero_ctx* ctx);
  * release.  With a hook registered the gathers run on stream_gather, so the
  * next unit's gather overlaps the work on the current one (prefetch); with
  * none, everything runs in order on stream_update (there is no compute to
- * hide a gather behind) and each backward gather is done by the unit's
+ * hide a gather behind): the forward pass gathers two units per launch, one
+ * into each unit buffer, and each backward gather is done by the unit's
  * update pass, which copies the unit's 16-bit values into the unit buffer
  * before overwriting them.  At most two unit buffers are live.  Traffic:
  * 3 (W-1) S_u 2 bytes per unit.
@@ -430,8 +431,8 @@ int zero_set_variant(zero_ctx* ctx, int variant);
 /*
  * ZeRO-3 steps from a CUDA graph (on != 0) or as ordinary launches (0, the
  * default).  With it on, the first zero_step that runs without a unit hook,
- * timing brackets, debug flags or an injected stall captures its 2 U
- * launches into a graph; that step and every later one with the same
+ * timing brackets, debug flags or an injected stall captures its U + U/2
+ * launches (rounded up) into a graph; that step and every later one with the same
  * conditions set the fused kernels' Adam coefficients and gradient pointers
  * on the graph and launch it once on the update stream, which saves the gaps
  * between the launches.  Steps under other conditions run the ordinary

@@ -207,12 +207,19 @@ int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const zero::
 }
 
 int launch_gather(zero_ctx* c, int64_t u, void* dst, cudaStream_t stream) {
-  const int64_t S = c->L.shard[u];
+  return launch_gathers(c, &u, &dst, 1, stream);
+}
+
+int launch_gathers(zero_ctx* c, const int64_t* units, void* const* dsts, int count, cudaStream_t stream) {
   std::vector<zero::CopySeg> segs;
-  for (int r = 0; r < c->W && S > 0; ++r) {
-    const char* src = static_cast<const char*>(c->shard16[r]) + c->L.off16[u] * 2;
-    segs.push_back({src, static_cast<char*>(dst) + r * S * 2, S * 2});
+  for (int k = 0; k < count; ++k) {
+    const int64_t u = units[k], S = c->L.shard[u];
+    for (int r = 0; r < c->W && S > 0; ++r) {
+      const char* src = static_cast<const char*>(c->shard16[r]) + c->L.off16[u] * 2;
+      segs.push_back({src, static_cast<char*>(dsts[k]) + r * S * 2, S * 2});
+    }
   }
+  if (segs.empty()) return ZERO_OK;
   Bracket br{c, ZERO_KERNEL_GATHER, stream};
   int rc = br.open();
   if (rc) return rc;
@@ -342,9 +349,33 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
     used[b] = true;
     return ZERO_OK;
   };
-  for (int64_t u = 0; u < U; ++u) {
-    rc = unit(u, 0);
-    if (rc) return rc;
+  if (c->hook == nullptr && 2 * c->W <= zero::kMaxCopySegs) {
+    // Nothing runs between the forward gathers, so two units (one into each
+    // buffer) go in one launch: the same copies in half the launches.
+    for (int64_t u = 0; u < U; u += 2) {
+      Range range("zero3 forward units %lld+", static_cast<long long>(u));
+      const int count = U - u >= 2 ? 2 : 1;
+      int64_t us[2];
+      void* dsts[2];
+      for (int k = 0; k < count; ++k) {
+        const int b = static_cast<int>(seq++ & 1);
+        c->live_elems -= held[b];
+        held[b] = c->L.shard[u + k] * c->W;
+        live_add(c, held[b]);
+        count_gather(c, u + k);
+        us[k] = u + k;
+        dsts[k] = c->ubuf[b];
+        used[b] = true;
+      }
+      if ((rc = launch_gathers(c, us, dsts, count, su))) return rc;
+      for (int k = 0; k < count; ++k)
+        if ((rc = poison_unit(c, us[k], dsts[k], su))) return rc;
+    }
+  } else {
+    for (int64_t u = 0; u < U; ++u) {
+      rc = unit(u, 0);
+      if (rc) return rc;
+    }
   }
   for (int64_t u = U - 1; u >= 0; --u) {
     rc = unit(u, 1);

@@ -167,8 +167,10 @@ AdamCoef make_coef(double lr, double b1, double b2, double eps, int64_t t, int W
 int launch_update(zero_ctx* c, int64_t u, const void* const* grads, const AdamCoef& coef, cudaStream_t stream,
                   void* gather_dst = nullptr, int64_t lo = 0, int64_t len = -1);
 
-// Gather unit u's 16-bit shards into dst, in flat order.
+// Gather unit u's 16-bit shards into dst, in flat order; launch_gathers does
+// `count` units (each into its own buffer) in one launch.
 int launch_gather(zero_ctx* c, int64_t u, void* dst, cudaStream_t stream);
+int launch_gathers(zero_ctx* c, const int64_t* units, void* const* dsts, int count, cudaStream_t stream);
 
 // Counters: gathers, reduce-scatters and traffic, gathered elements live.
 void count_gather(zero_ctx* c, int64_t u);
