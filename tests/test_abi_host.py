@@ -301,3 +301,47 @@ def test_graph_mode_checks(zlib):
     z3 = make_ctx(scheme=3, W=4, units=(37, 5))
     assert _err(zs.zero_set_graph, z3, True) == zs.ZERO_E_ARG   # no stream: the legacy default stream
     assert "legacy" in zs.zero_last_error()
+
+
+def declared_prototypes():
+    """name -> (return type, [parameter types]) for every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"#.*", "", text)
+    protos = {}
+    for ret, name, params in re.findall(r"((?:const\s+)?[a-z_0-9]+\s*\**)\s*(zero_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text,
+                                        flags=re.S):
+        params = " ".join(params.split())
+        plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        protos[name] = (" ".join(ret.split()), plist)
+    return protos
+
+
+def _ctype_of(decl: str):
+    """The ctypes type a C parameter or return declaration maps to in the binding."""
+    m = re.match(r"^(.*?[\s*])([A-Za-z_][A-Za-z_0-9]*)$", decl.strip())   # drop the parameter's name
+    base = (m.group(1) if m else decl).replace("const", "").replace(" ", "")
+    table = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "double": ctypes.c_double,
+             "int64_t*": ctypes.POINTER(ctypes.c_int64), "double*": ctypes.POINTER(ctypes.c_double),
+             "int*": ctypes.POINTER(ctypes.c_int), "char*": ctypes.c_char_p,
+             "zero_unit_hook": zs.HOOK, "void**": zs._PP, "float**": zs._PP,
+             "zero_ctx**": ctypes.POINTER(ctypes.c_void_p), "zero_offload**": ctypes.POINTER(ctypes.c_void_p)}
+    if base in table:
+        return table[base]
+    if base.endswith("*"):
+        return ctypes.c_void_p
+    raise AssertionError(f"no mapping for {decl!r}")
+
+
+def test_binding_signatures_match_the_header():
+    """Every wrapper's ctypes argument and return types follow the header's
+    prototype, argument by argument (a mismatch would corrupt calls silently)."""
+    protos = declared_prototypes()
+    assert set(protos) == set(zs.SIGNATURES)
+    for name, (ret, params) in protos.items():
+        res, args = zs.SIGNATURES[name]
+        assert len(args) == len(params), (name, params, args)
+        for p, a in zip(params, args):
+            # a pointer may also be passed as a raw address (device memory, tensors' data_ptr())
+            raw_ok = "*" in p and a is ctypes.c_void_p
+            assert raw_ok or _ctype_of(p) == a, (name, p, a)
+        assert _ctype_of(ret + " x" if not ret.endswith("*") else ret) == res, (name, ret, res)
