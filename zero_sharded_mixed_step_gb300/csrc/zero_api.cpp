@@ -295,9 +295,11 @@ int poison_unit(zero_ctx* c, int64_t u, void* buf, cudaStream_t s) {
 // behind the caller's compute on the unit before it, so it is used when a
 // unit hook is registered; with no hook the only work on stream A is the
 // memory-bound update, and running the gathers beside it on GB300 measured
-// slower than running everything in order on stream A.  A unit counts as live
-// from its gather until its buffer is taken by a later gather (or the step
-// ends): at most two units are live.
+// slower than running everything in order on stream A.  Without a hook the
+// forward gathers also go two units per launch (one into each buffer), and
+// each backward gather is done by its unit's update pass.  A unit counts as
+// live from its gather until its buffer is taken by a later gather (or the
+// step ends): at most two units are live.
 int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& coef) {
   int rc = ensure_cuda(c);
   if (rc) return rc;
