@@ -30,6 +30,7 @@
 // host, by design of the offloaded step; no GPU entry point falls back to it.
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -361,6 +362,11 @@ extern "C" int zero_offload_step(zero_offload* c, const void* const* grads, doub
   }
   const zero::AdamCoef coef = zero::adam_coef(lr, beta1, beta2, eps, t, c->W);
   a.inv_w = coef.inv_w;
+  // NVTX ranges on the host timeline: the whole step, and its host phase
+  struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+  } step_range("zero_offload_step");
   cudaError_t e = cudaSuccess;
   // everything on the device side, up front
   for (int64_t k = 0; k < c->n_chunks && e == cudaSuccess; ++k) {
@@ -396,6 +402,7 @@ extern "C" int zero_offload_step(zero_offload* c, const void* const* grads, doub
   FirstError err;
   uint16_t* const dev16 = static_cast<uint16_t*>(c->p16);
   const auto t0 = std::chrono::steady_clock::now();
+  nvtxRangePushA("zero_offload_step host update");
   c->pool->run(pieces, 1, [&](int64_t p0, int64_t p1) {
     for (int64_t p = p0; p < p1; ++p) {
       if (err.code.load() != ZERO_OK) return;
@@ -425,6 +432,7 @@ extern "C" int zero_offload_step(zero_offload* c, const void* const* grads, doub
       }
     }
   });
+  nvtxRangePop();
   c->host_seconds += std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
   if (err.code.load() != ZERO_OK) return fail(err.code.load(), err.msg);
   c->h2d_bytes += c->n_pad * 2;
