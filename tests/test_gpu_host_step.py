@@ -124,3 +124,47 @@ def test_host_alloc_is_page_locked_aligned_and_zeroed():
     with pytest.raises(zs.ZeroError) as e:
         zs.zero_host_free(ptr)
     assert e.value.code == zs.ZERO_E_ARG
+
+
+def test_host_step_with_the_benchmark_units():
+    """The benchmark's ZeRO-3 units (50,331,648 parameters on 8 ranks; the first
+    three of its 24, to keep the test's host memory small) fed from host
+    memory the way the benchmark's end-to-end leg feeds them (one huge-page
+    block for the W gradient vectors and the read-back): two steps,
+    bit-identical to the device step, the read-back equal to the device's
+    shard stores."""
+    wl = wk.scaled(wk.LAYER_UNITS, unit_sizes=wk.LAYER_UNITS.unit_sizes[:3], steps=2)
+    units, W = wl.units(), wl.W
+    theta0 = wk.draw_theta0(wl, "cuda")
+    a = zs.ZeroStep(zs.ZERO_SCHEME_Z3, W, units, "bf16", theta0=theta0, with_grad_buffers=True)
+    b = zs.ZeroStep(zs.ZERO_SCHEME_Z3, W, units, "bf16", theta0=theta0)
+    del theta0
+    n_pad, out_elems = a.n_pad, W * a.sizes["shard_store"]
+    block = zs.HostBuffer(W * n_pad + out_elems, torch.int16)
+    host = [block.tensor[r * n_pad:(r + 1) * n_pad].view(torch.bfloat16) for r in range(W)]
+    host_out = block.tensor[W * n_pad:].view(torch.bfloat16)
+    need = zs.zero_host_staging_bytes(zs.ZERO_SCHEME_Z3, W, units, 0)
+    staging = torch.empty(need, dtype=torch.uint8, device="cuda")
+    sh, sd = torch.cuda.Stream(), torch.cuda.Stream()
+    src = wk.GradSource(wl, "bf16", "cuda")
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    for t in range(1, wl.steps + 1):
+        for g, d in zip(a.grads, src.step(t)):
+            a.place_(g, d)
+        for h, g in zip(host, a.grads):
+            h.copy_(g)
+        torch.cuda.synchronize()
+        a.step(a.grads, *hp, t)
+        zs.zero_step_host(b.ctx, zs.ZERO_SCHEME_Z3, W, wl.n, host, host_out, staging, need, 0, *hp, t, sh, sd)
+        b.sync(timeout_ms=120_000)
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
+        want = torch.cat([x.cpu() for x in b.shard16])
+        assert torch.equal(host_out.view(torch.int16), want.view(torch.int16)), t
+        for x, y in zip(a.shard16, b.shard16):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16)), t
+    assert a.stat(zs.ZERO_STAT_COMM_BYTES) == b.stat(zs.ZERO_STAT_COMM_BYTES)
+    del host, host_out
+    block.close()
+    a.close()
+    b.close()
