@@ -89,3 +89,40 @@ def test_oracle_host_memory_check_refuses_what_does_not_fit(monkeypatch):
         bench.check_host_memory(bench.oracle_bytes(wl, wl.n) * 1000, "the whole GPT-2-1.5B vector, 1000 times")
     # literal DP replicas cost the oracle W copies of the state
     assert bench.oracle_bytes(wk.GPT2_SMALL_DP_REPLICAS, 1000) > bench.oracle_bytes(wk.GPT2_SMALL, 1000)
+
+
+def test_settled_host_block_retries_split_blocks(monkeypatch):
+    """A block whose huge pages were split by the probe is kept aside while a
+    new one is taken (at most three); the fastest is used, the rest freed."""
+    import torch
+    import zero_sharded_mixed_step_gb300 as zs
+
+    made, closed = [], []
+
+    class FakeBlock:
+        def __init__(self, numel, dtype):
+            self.tensor = torch.zeros(numel, dtype=dtype)
+            self.index = len(made)
+            made.append(self)
+
+        def close(self):
+            closed.append(self.index)
+
+    fractions = {0: 0.9, 1: 0.96, 2: 1.0}
+    rates = {0: 40.0, 1: 120.0, 2: 211.0}
+    monkeypatch.setattr(zs, "HostBuffer", FakeBlock)
+    monkeypatch.setattr(bench, "huge_page_fraction", lambda bufs: fractions[bufs[0].index])
+    probes = []
+
+    def probe_of(views):
+        probes.append(views)
+        return {"h2d_gbs": rates[len(probes) - 1]}
+
+    block, views, probe = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
+    assert block.index == 2 and probe["host_block_attempts"] == 3 and probe["h2d_gbs"] == 211.0
+    assert sorted(closed) == [0, 1]
+    # a block that keeps its huge pages is taken at once
+    made.clear(), closed.clear(), probes.clear()
+    fractions[0] = 1.0
+    block, views, probe = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
+    assert block.index == 0 and probe["host_block_attempts"] == 1 and closed == []
