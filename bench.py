@@ -515,7 +515,8 @@ def run_ours(args):
                 back = [(out_h[r * S16:(r + 1) * S16], step.shard16[r]) for r in range(wl.W)]
             return link_probe(list(zip(step.grads, grads_h)), back, sh)
 
-        block_buf, (host_grads, host_out), link = settled_host_block(wl.W * step.n_pad + out_elems, views_of, probe_of)
+        block_buf, (host_grads, host_out), link, spares = settled_host_block(wl.W * step.n_pad + out_elems,
+                                                                             views_of, probe_of)
         host_bufs = [block_buf]
 
         def host_step():
@@ -528,20 +529,23 @@ def run_ours(args):
         step.sync()
         if world > 1:
             dist.barrier()
+        marks = StepMarks(sd)            # each step ends with its read-back on sd
         h0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             host_step()
+            marks.mark()
         step.sync()
         e2e_s = max_over_ranks(time.perf_counter() - h0)
+        link["after"] = after_e2e(probe_of, (host_grads, host_out), host_bufs)
         h2d = sum(h.numel() * h.element_size() for h in host_grads)
         d2h = host_out.numel() * host_out.element_size()
         e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-               "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "staging_bytes": need,
+               "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "step_ms": marks.spread(), "staging_bytes": need,
                "path": "zero_step_host: host gradients (zero_host_alloc) -> 2-slot device staging ring -> "
                        "fused step -> 16-bit working copy -> host, pipelined over three streams", "link": link}
         del host_grads, host_out, staging
-        for b in host_bufs:
+        for b in host_bufs + spares:
             b.close()
 
     step.close()
@@ -590,6 +594,40 @@ def link_probe(h2d_pairs, d2h_pairs, stream):
                     "floor = the step's gradients carried in at that rate"}
 
 
+class StepMarks:
+    """CUDA events on the stream that ends each end-to-end step: one before
+    the first timed step and one after each, so that the steps' own
+    durations can be read without a host synchronisation between them."""
+
+    def __init__(self, stream):
+        import torch
+        self.stream = stream
+        self.events = [torch.cuda.Event(enable_timing=True)]
+        self.events[0].record(stream)
+
+    def mark(self):
+        import torch
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        self.events.append(e)
+
+    def spread(self):
+        """min / median / max of the marked steps' durations, ms (after a sync)."""
+        ms = sorted(a.elapsed_time(b) for a, b in zip(self.events, self.events[1:]))
+        if not ms:
+            return None
+        return {"min": ms[0], "median": ms[len(ms) // 2], "max": ms[-1]}
+
+
+def after_e2e(probe_of, views, bufs):
+    """The link probe and the huge-page share once more, after the timed
+    end-to-end steps: a slow run whose link was slow too was slowed by the
+    link (shared with other jobs), one whose link was fast by the pipeline."""
+    probe = probe_of(views)
+    return {"h2d_gbs": probe["h2d_gbs"], "d2h_gbs": probe["d2h_gbs"],
+            "host_huge_page_fraction": huge_page_fraction(bufs)}
+
+
 def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
     """A zero_host_alloc block of ``elems16`` 16-bit elements whose pages are
     still all huge after a first round of the step's copies.
@@ -601,8 +639,15 @@ def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
     of the split pages run at a fraction of the link's rate.  A block that
     comes out of its probe with split pages is kept aside (so that its pages
     are not handed out again) while a new one is taken, at most ``attempts``
-    times; the block with the fastest probe is used and the others are freed.
-    Returns (block, views, probe) with the attempts recorded in the probe."""
+    times.  The block that kept the most of its huge pages is used (the
+    fastest probe among equals: a block whose pages have begun to split
+    goes on splitting under later copies, even when its probe was still
+    fast).  The others come back
+    as spares for the caller to free once its timed steps are over: freeing
+    tens of GB of pinned memory just before them set the kernel splitting the
+    chosen block's huge pages while they ran.
+    Returns (block, views, probe, spares) with the attempts recorded in the
+    probe."""
     import torch
     import zero_sharded_mixed_step_gb300 as zs
     tried = []
@@ -616,13 +661,10 @@ def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
         tried.append((hb, views, probe))
         if probe["host_huge_page_fraction"] is None or probe["host_huge_page_fraction"] >= 0.999:
             break
-    best = max(tried, key=lambda x: x[2]["h2d_gbs"])
-    for hb, views, _ in tried:
-        if hb is not best[0]:
-            del views
-            hb.close()
+    best = max(tried, key=lambda x: (x[2]["host_huge_page_fraction"] or 0.0, x[2]["h2d_gbs"]))
     best[2]["host_block_attempts"] = len(tried)
-    return best
+    spares = [hb for hb, _, _ in tried if hb is not best[0]]
+    return best[0], best[1], best[2], spares
 
 
 def huge_page_fraction(bufs) -> float | None:
@@ -677,7 +719,7 @@ def e2e_through_torch_copies(args, world, wl, su, grads, result, run_step, t0, p
         grads_h, out_h = views
         return link_probe(list(zip(grads, grads_h)), [(out_h, result)], su)
 
-    block_buf, (host_grads, host_out), link = settled_host_block(W * n + result.numel(), views_of, probe_of)
+    block_buf, (host_grads, host_out), link, spares = settled_host_block(W * n + result.numel(), views_of, probe_of)
     host_bufs = [block_buf]
     t = t0
 
@@ -695,17 +737,20 @@ def e2e_through_torch_copies(args, world, wl, su, grads, result, run_step, t0, p
     su.synchronize()
     if world > 1:
         dist.barrier()
+    marks = StepMarks(su)
     h0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         host_step()
+        marks.mark()
     su.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - h0)
+    link["after"] = after_e2e(probe_of, (host_grads, host_out), host_bufs)
     e2e = {"value": whole_job_value(world, wl.n, args.e2e_steps, 1e3 * e2e_s), "unit": "params/s",
            "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
            "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": args.e2e_steps,
-           "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "path": path, "link": link}
+           "ms_per_step": 1e3 * e2e_s / args.e2e_steps, "step_ms": marks.spread(), "path": path, "link": link}
     del host_grads, host_out
-    for b in host_bufs:
+    for b in host_bufs + spares:
         b.close()
     return e2e, t
 

@@ -93,7 +93,9 @@ def test_oracle_host_memory_check_refuses_what_does_not_fit(monkeypatch):
 
 def test_settled_host_block_retries_split_blocks(monkeypatch):
     """A block whose huge pages were split by the probe is kept aside while a
-    new one is taken (at most three); the fastest is used, the rest freed."""
+    new one is taken (at most three); the one with the most huge pages (then
+    the fastest) is used and the rest come back as spares, still open, for
+    the caller to free after its timed steps."""
     import torch
     import zero_sharded_mixed_step_gb300 as zs
 
@@ -118,11 +120,32 @@ def test_settled_host_block_retries_split_blocks(monkeypatch):
         probes.append(views)
         return {"h2d_gbs": rates[len(probes) - 1]}
 
-    block, views, probe = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
+    block, views, probe, spares = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
     assert block.index == 2 and probe["host_block_attempts"] == 3 and probe["h2d_gbs"] == 211.0
-    assert sorted(closed) == [0, 1]
+    assert sorted(b.index for b in spares) == [0, 1] and closed == []
     # a block that keeps its huge pages is taken at once
     made.clear(), closed.clear(), probes.clear()
     fractions[0] = 1.0
-    block, views, probe = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
-    assert block.index == 0 and probe["host_block_attempts"] == 1 and closed == []
+    block, views, probe, spares = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
+    assert block.index == 0 and probe["host_block_attempts"] == 1 and spares == [] and closed == []
+    # a block whose pages began to split loses to an intact one, however fast its probe
+    made.clear(), closed.clear(), probes.clear()
+    fractions.update({0: 0.96, 1: 1.0})
+    rates.update({0: 211.5, 1: 211.4})
+    block, views, probe, spares = bench.settled_host_block(64, lambda t: ("views", t.numel()), probe_of)
+    assert block.index == 1 and probe["host_block_attempts"] == 2 and [b.index for b in spares] == [0]
+
+
+def test_after_e2e_reports_the_link_and_pages_once_more(monkeypatch):
+    """The second probe after the timed end-to-end steps carries the link
+    rates and the huge-page share at that point."""
+    monkeypatch.setattr(bench, "huge_page_fraction", lambda bufs: 0.5)
+    seen = []
+
+    def probe_of(views):
+        seen.append(views)
+        return {"h2d_gbs": 52.0, "d2h_gbs": 15.0, "floor_ms": 1.0, "note": "x"}
+
+    after = bench.after_e2e(probe_of, ("g", "o"), ["block"])
+    assert seen == [("g", "o")]
+    assert after == {"h2d_gbs": 52.0, "d2h_gbs": 15.0, "host_huge_page_fraction": 0.5}
