@@ -422,6 +422,7 @@ int capture_zero3(zero_ctx* c, const void* const* grads, const zero::AdamCoef& c
     c->err_slot_ready = true;
   }
   const int64_t comm = c->comm, launches = c->launches, gathers = c->gathers, scatters = c->scatters;
+  const int64_t live = c->live_elems, peak = c->peak_live;
   ZERO_CUDA(cudaStreamBeginCapture(c->su, cudaStreamCaptureModeThreadLocal));
   rc = run_zero3_step(c, grads, coef);
   cudaGraph_t g = nullptr;
@@ -435,6 +436,9 @@ int capture_zero3(zero_ctx* c, const void* const* grads, const zero::AdamCoef& c
   c->gathers = gathers;
   c->scatters = scatters;
   if (rc || e != cudaSuccess) {
+    // a step that failed part way leaves the unit counters as they were
+    c->live_elems = live;
+    c->peak_live = peak;
     if (g) cudaGraphDestroy(g);
     return rc ? rc : cuda_fail(e, "capturing the ZeRO-3 step");
   }

@@ -115,7 +115,7 @@ struct zero_ctx {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t graph_exec = nullptr;
   std::vector<std::pair<cudaGraphNode_t, zero::FusedLaunch>> graph_fused;
-  int64_t graph_comm = 0, graph_launches = 0, graph_gathers = 0, graph_scatters = 0, graph_peak = 0;
+  int64_t graph_comm = 0, graph_launches = 0, graph_gathers = 0, graph_scatters = 0;
 };
 
 namespace zero {
