@@ -408,11 +408,13 @@ class ZeroStep:
 
     ``theta0`` (n fp32 values, any device) is written to the real positions
     of the padded master; m and v start at zero; the 16-bit working copy is
-    cast from the master before the first step.
+    cast from the master before the first step.  ``alloc(numel, dtype)``, if
+    given, supplies every device buffer instead of ``torch.zeros`` (a
+    zero-filled tensor on ``device``, e.g. from the caller's own pool).
     """
 
     def __init__(self, scheme, W, unit_sizes, grad_dtype="fp16", work_dtype=None, theta0=None,
-                 device="cuda", stream=None, gather_stream=None, with_grad_buffers=False):
+                 device="cuda", stream=None, gather_stream=None, with_grad_buffers=False, alloc=None):
         import torch
         self.torch = torch
         self.scheme, self.W = int(scheme), int(W)
@@ -425,15 +427,15 @@ class ZeroStep:
         self.device = torch.device(device)
         t16 = {ZERO_FP16: torch.float16, ZERO_BF16: torch.bfloat16}
         self.grad_torch_dtype, self.work_torch_dtype = t16[self.gdt], t16[self.wdt]
-        f32 = dict(dtype=torch.float32, device=self.device)
-        self.master = torch.zeros(self.n_pad, **f32)
-        self.m = torch.zeros(self.n_pad, **f32)
-        self.v = torch.zeros(self.n_pad, **f32)
-        w16 = dict(dtype=self.work_torch_dtype, device=self.device)
-        self.p16 = torch.zeros(self.sizes["p16"], **w16) if self.scheme != ZERO_SCHEME_Z3 else None
-        self.shard16 = ([torch.zeros(self.sizes["shard_store"], **w16) for _ in range(self.W)]
+        self._alloc = alloc or (lambda numel, dtype: torch.zeros(numel, dtype=dtype, device=self.device))
+        f32, w16 = torch.float32, self.work_torch_dtype
+        self.master = self._alloc(self.n_pad, f32)
+        self.m = self._alloc(self.n_pad, f32)
+        self.v = self._alloc(self.n_pad, f32)
+        self.p16 = self._alloc(self.sizes["p16"], w16) if self.scheme != ZERO_SCHEME_Z3 else None
+        self.shard16 = ([self._alloc(self.sizes["shard_store"], w16) for _ in range(self.W)]
                         if self.scheme == ZERO_SCHEME_Z3 else None)
-        self.unit_bufs = ([torch.zeros(self.sizes["unit_buf"], **w16) for _ in range(2)]
+        self.unit_bufs = ([self._alloc(self.sizes["unit_buf"], w16) for _ in range(2)]
                           if self.scheme == ZERO_SCHEME_Z3 else None)
         if theta0 is not None:
             self.place_(self.master, theta0)
@@ -463,7 +465,7 @@ class ZeroStep:
         return dst
 
     def new_grad_buffers(self):
-        return [self.torch.zeros(self.n_pad, dtype=self.grad_torch_dtype, device=self.device) for _ in range(self.W)]
+        return [self._alloc(self.n_pad, self.grad_torch_dtype) for _ in range(self.W)]
 
     def working_copy(self):
         """The full 16-bit vector in flat order (Z3: every rank's shards interleaved back)."""
@@ -515,10 +517,11 @@ class DpReplicas:
     ``theta0`` (n fp32 values) is written into every replica's master; m and
     v start at zero.  Each 16-bit working copy is written by the step (it
     holds zeros before the first one).  The step and the replica check run
-    in the library.
+    in the library.  ``alloc`` as for :class:`ZeroStep`.
     """
 
-    def __init__(self, W, n, grad_dtype="fp16", work_dtype=None, theta0=None, device="cuda", stream=None):
+    def __init__(self, W, n, grad_dtype="fp16", work_dtype=None, theta0=None, device="cuda", stream=None,
+                 alloc=None):
         import torch
         self.torch = torch
         self.W, self.n = int(W), int(n)
@@ -534,20 +537,20 @@ class DpReplicas:
             if need > free:
                 raise MemoryError(f"{self.W} replicas of {self.n_pad} parameters need {need} bytes of device "
                                   f"memory; {free} are free")
-        f32 = dict(dtype=torch.float32, device=self.device)
-        self.master = [torch.zeros(self.n_pad, **f32) for _ in range(self.W)]
-        self.m = [torch.zeros(self.n_pad, **f32) for _ in range(self.W)]
-        self.v = [torch.zeros(self.n_pad, **f32) for _ in range(self.W)]
-        self.p16 = [torch.zeros(self.n_pad, dtype=self.work_torch_dtype, device=self.device) for _ in range(self.W)]
+        self._alloc = alloc or (lambda numel, dtype: torch.zeros(numel, dtype=dtype, device=self.device))
+        self.master = [self._alloc(self.n_pad, torch.float32) for _ in range(self.W)]
+        self.m = [self._alloc(self.n_pad, torch.float32) for _ in range(self.W)]
+        self.v = [self._alloc(self.n_pad, torch.float32) for _ in range(self.W)]
+        self.p16 = [self._alloc(self.n_pad, self.work_torch_dtype) for _ in range(self.W)]
         if theta0 is not None:
             th = torch.as_tensor(theta0).to(device=self.device, dtype=torch.float32)
             for r in range(self.W):
                 self.master[r][: self.n].copy_(th)
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
-        self._count = torch.zeros(1, dtype=torch.int64, device=self.device)
+        self._count = self._alloc(1, torch.int64)
 
     def new_grad_buffers(self):
-        return [self.torch.zeros(self.n_pad, dtype=self.grad_torch_dtype, device=self.device) for _ in range(self.W)]
+        return [self._alloc(self.n_pad, self.grad_torch_dtype) for _ in range(self.W)]
 
     def step(self, grads, lr, beta1, beta2, eps, t):
         zero_step_dp_replicas(self.W, self.n, self.gdt, self.wdt, grads, self.master, self.m, self.v, self.p16,
@@ -566,10 +569,13 @@ class ZeroOffload:
     memory (the 16-bit working copy and the gradients on ``device``), the
     fp32 means and 16-bit results crossing the link through page-locked
     buffers from ``zero_host_alloc``.  ``theta0`` (n values) seeds the
-    master; the device working copy is written by each step."""
+    master; the device working copy is written by each step.  ``alloc`` as
+    for :class:`ZeroStep`; ``host_alloc(numel, dtype)``, if given, supplies
+    the five host buffers (zero-filled CPU tensors, best page-locked)
+    instead of ``zero_host_alloc``."""
 
     def __init__(self, W, n, grad_dtype="fp16", work_dtype=None, theta0=None, device="cuda", stream=None,
-                 chunk_elems=0, threads=0):
+                 chunk_elems=0, threads=0, alloc=None, host_alloc=None):
         import torch
         self.torch = torch
         self.W, self.n = int(W), int(n)
@@ -579,22 +585,26 @@ class ZeroOffload:
         self.device = torch.device(device)
         t16 = {ZERO_FP16: torch.float16, ZERO_BF16: torch.bfloat16}
         self.grad_torch_dtype, self.work_torch_dtype = t16[self.gdt], t16[self.wdt]
-        self._bufs = [HostBuffer(self.n_pad, torch.float32) for _ in range(4)]
-        self.master, self.m, self.v, self.host_grad = (b.tensor for b in self._bufs)
-        self._bufs.append(HostBuffer(self.n_pad, self.work_torch_dtype))
-        self.host_p16 = self._bufs[-1].tensor
+        self._bufs = []
+        if host_alloc is None:
+            def host_alloc(numel, dtype):
+                self._bufs.append(HostBuffer(numel, dtype))
+                return self._bufs[-1].tensor
+        self.master, self.m, self.v, self.host_grad = (host_alloc(self.n_pad, torch.float32) for _ in range(4))
+        self.host_p16 = host_alloc(self.n_pad, self.work_torch_dtype)
         if theta0 is not None:
             self.master[: self.n].copy_(torch.as_tensor(theta0, dtype=torch.float32).cpu())
-        self.p16 = torch.zeros(self.n_pad, dtype=self.work_torch_dtype, device=self.device)
+        self._alloc = alloc or (lambda numel, dtype: torch.zeros(numel, dtype=dtype, device=self.device))
+        self.p16 = self._alloc(self.n_pad, self.work_torch_dtype)
         self.staging_bytes = zero_offload_staging_bytes(chunk_elems)
-        self.staging = torch.empty(self.staging_bytes, dtype=torch.uint8, device=self.device)
+        self.staging = self._alloc(self.staging_bytes, torch.uint8)
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.ctx = zero_offload_init(self.W, self.n, self.gdt, self.wdt, self.master, self.m, self.v,
                                      self.host_grad, self.host_p16, self.p16, self.staging, self.staging_bytes,
                                      chunk_elems, threads, self.stream)
 
     def new_grad_buffers(self):
-        return [self.torch.zeros(self.n_pad, dtype=self.grad_torch_dtype, device=self.device) for _ in range(self.W)]
+        return [self._alloc(self.n_pad, self.grad_torch_dtype) for _ in range(self.W)]
 
     def step(self, grads, lr, beta1, beta2, eps, t):
         zero_offload_step(self.ctx, grads, lr, beta1, beta2, eps, t)
