@@ -916,7 +916,7 @@ def run_offload(args, wl, dtype, world, rank, dev):
                 "traffic": None, "kernel": "host Adam (zero_offload_step's host update)",
                 "peak_source": f"host copy measured in this run ({st1['threads']} threads, read + write)",
                 "host_ms_per_step": 1e3 * host_s, "algorithmic_bytes_per_step": host_bytes, "bytes_per_element": 30,
-                "threads": st1["threads"]}
+                "threads": st1["threads"], "host_state_huge_page_fraction": huge_page_fraction(off._bufs)}
     launches = st1["launches"] - st0["launches"]
     link = {"d2h_bytes_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.steps,
             "h2d_bytes_per_step": (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.steps}

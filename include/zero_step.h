@@ -581,6 +581,9 @@ int64_t zero_offload_staging_bytes(int64_t chunk_elems);
  *   host_grad    host memory for n_pad fp32 means; host_p16 host memory for
  *                n_pad 16-bit values.  Both should be page-locked (e.g. from
  *                zero_host_alloc) so that their copies run asynchronously.
+ *                Slicing all five host vectors from one zero_host_alloc block
+ *                puts them on huge pages even where each alone is smaller
+ *                than one; the host pass and the copies run faster there.
  *   p16          device, n_pad 16-bit values (work_dtype), 16-byte aligned:
  *                the working copy, overwritten by each step.
  *   staging      device, >= zero_offload_staging_bytes(chunk_elems) bytes,

@@ -564,6 +564,15 @@ class DpReplicas:
         return int(self._count.item())
 
 
+def _itemsize(dtype) -> int:
+    import torch
+    return torch.empty(0, dtype=dtype).element_size()
+
+
+def _round4k(nbytes: int) -> int:
+    return -(-int(nbytes) // 4096) * 4096
+
+
 class ZeroOffload:
     """ZeRO-2 with the optimizer on the host: fp32 master, m and v in host
     memory (the 16-bit working copy and the gradients on ``device``), the
@@ -586,12 +595,21 @@ class ZeroOffload:
         t16 = {ZERO_FP16: torch.float16, ZERO_BF16: torch.bfloat16}
         self.grad_torch_dtype, self.work_torch_dtype = t16[self.gdt], t16[self.wdt]
         self._bufs = []
+        specs = [(self.n_pad, torch.float32)] * 4 + [(self.n_pad, self.work_torch_dtype)]
         if host_alloc is None:
-            def host_alloc(numel, dtype):
-                self._bufs.append(HostBuffer(numel, dtype))
-                return self._bufs[-1].tensor
-        self.master, self.m, self.v, self.host_grad = (host_alloc(self.n_pad, torch.float32) for _ in range(4))
-        self.host_p16 = host_alloc(self.n_pad, self.work_torch_dtype)
+            # one zero_host_alloc block for all five: each vector alone can be
+            # smaller than a huge page, and such blocks stay on base pages, over
+            # which the host pass and the link copies both measured slower
+            block = HostBuffer(max(1, sum(_round4k(numel * _itemsize(d)) for numel, d in specs)), torch.uint8)
+            self._bufs.append(block)
+            views, pos = [], 0
+            for numel, dtype in specs:
+                nbytes = numel * _itemsize(dtype)
+                views.append(block.tensor[pos:pos + nbytes].view(dtype))
+                pos += _round4k(nbytes)
+        else:
+            views = [host_alloc(numel, dtype) for numel, dtype in specs]
+        self.master, self.m, self.v, self.host_grad, self.host_p16 = views
         if theta0 is not None:
             self.master[: self.n].copy_(torch.as_tensor(theta0, dtype=torch.float32).cpu())
         self._alloc = alloc or (lambda numel, dtype: torch.zeros(numel, dtype=dtype, device=self.device))
