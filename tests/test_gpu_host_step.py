@@ -3,7 +3,6 @@ against zero_step on the same gradients (GPU needed)."""
 
 import os
 
-import numpy as np
 import pytest
 import torch
 

@@ -2,7 +2,6 @@
 bitwise against the device step zero_step on the same gradients, and
 against the oracle."""
 
-import numpy as np
 import pytest
 import torch
 
