@@ -220,10 +220,8 @@ def oracle_bytes(wl, elems: int) -> int:
 
 def check_host_memory(need: int, what: str) -> None:
     """Fail with a clear message, before allocating, when the host cannot hold ``need`` bytes."""
-    try:
-        with open("/proc/meminfo") as f:
-            avail = next(int(line.split()[1]) * 1024 for line in f if line.startswith("MemAvailable:"))
-    except (OSError, StopIteration):
+    avail = host_mem_available()
+    if avail is None:
         return
     if need > avail:
         raise MemoryError(f"{what} needs about {need / 1e9:.1f} GB of host memory; {avail / 1e9:.1f} GB available")
@@ -652,7 +650,18 @@ def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
     import zero_sharded_mixed_step_gb300 as zs
     tried = []
     for _ in range(attempts):
-        hb = zs.HostBuffer(elems16, torch.int16)
+        if tried:
+            # another block only while the host keeps room for two more
+            # (several ranks on one host each hold their own blocks)
+            avail = host_mem_available()
+            if avail is not None and avail < 2 * 2 * elems16:
+                break
+            try:
+                hb = zs.HostBuffer(elems16, torch.int16)
+            except zs.ZeroError:
+                break
+        else:
+            hb = zs.HostBuffer(elems16, torch.int16)
         at_alloc = huge_page_fraction([hb])
         views = views_of(hb.tensor)
         probe = probe_of(views)
@@ -665,6 +674,17 @@ def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
     best[2]["host_block_attempts"] = len(tried)
     spares = [hb for hb, _, _ in tried if hb is not best[0]]
     return best[0], best[1], best[2], spares
+
+
+def host_mem_available() -> int | None:
+    """MemAvailable of /proc/meminfo in bytes (None where unreadable)."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
 
 
 def huge_page_fraction(bufs) -> float | None:

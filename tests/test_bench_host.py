@@ -149,3 +149,42 @@ def test_after_e2e_reports_the_link_and_pages_once_more(monkeypatch):
     after = bench.after_e2e(probe_of, ("g", "o"), ["block"])
     assert seen == [("g", "o")]
     assert after == {"h2d_gbs": 52.0, "d2h_gbs": 15.0, "host_huge_page_fraction": 0.5}
+
+
+def test_settled_host_block_stops_retrying_when_memory_runs_short(monkeypatch):
+    """A split block is still used when the host has no room for another one,
+    or when taking another one fails."""
+    import torch
+    import zero_sharded_mixed_step_gb300 as zs
+
+    made = []
+
+    class FakeBlock:
+        def __init__(self, numel, dtype):
+            if fail_next:
+                raise zs.ZeroError(zs.ZERO_E_NOMEM, "zero_host_alloc", "mmap failed")
+            self.tensor = torch.zeros(numel, dtype=dtype)
+            made.append(self)
+
+        def close(self):
+            pass
+
+    monkeypatch.setattr(zs, "HostBuffer", FakeBlock)
+    monkeypatch.setattr(bench, "huge_page_fraction", lambda bufs: 0.5)
+    probe_of = lambda views: {"h2d_gbs": 100.0}   # noqa: E731
+    fail_next = False
+    monkeypatch.setattr(bench, "host_mem_available", lambda: 3 * 64)      # less than two more blocks of 128 B
+    block, _, probe, spares = bench.settled_host_block(64, lambda t: None, probe_of)
+    assert probe["host_block_attempts"] == 1 and spares == [] and len(made) == 1
+    made.clear()
+    monkeypatch.setattr(bench, "host_mem_available", lambda: None)
+    real_init = FakeBlock.__init__
+
+    def init_then_fail(self, numel, dtype):
+        nonlocal fail_next
+        real_init(self, numel, dtype)
+        fail_next = True
+
+    monkeypatch.setattr(FakeBlock, "__init__", init_then_fail)
+    block, _, probe, spares = bench.settled_host_block(64, lambda t: None, probe_of)
+    assert probe["host_block_attempts"] == 1 and spares == [] and len(made) == 1
