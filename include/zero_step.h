@@ -215,6 +215,8 @@ int zero_refresh_working_copy(zero_ctx* ctx);
  *   grads             host array of W device pointers; rank w's gradients,
  *                     n_pad values of grad_dtype in flat order, read only.
  *   lr, beta1, beta2, eps  Adam hyper-parameters (0 <= beta < 1, eps > 0).
+ *          The update runs in fp32, so eps must also be a positive finite
+ *          fp32 value and lr / (1 - beta1^t) finite in fp32 (ZERO_E_ARG).
  *   t                 the step counter, 1-based: must be the context's last
  *                     step counter + 1 (ZERO_E_STATE otherwise).
  * DP/Z1/Z2: one fused pass over the flat vector: mean of the W gradients,

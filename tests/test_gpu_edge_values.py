@@ -2,12 +2,14 @@
 beyond the fp16 range (the working copy becomes +-inf, reading 5), gradients
 at the fp16 maximum, and all-zero gradients (nothing may move).  The device
 step, DP with literal replicas and the offloaded step must agree bit for bit
-and stay within the tolerance of the oracle."""
+and stay within the tolerance of the oracle.  Then the hyper-parameters at
+their edges, through the ZeRO-2 and ZeRO-3 kernels."""
 
 import numpy as np
 import pytest
 import torch
 
+import workloads as wk
 import zero_sharded_mixed_step_gb300 as zs
 from oracle import zero_oracle as z
 from tests.gpu_harness import assert_16bit_band, assert_f32_close, bits_of
@@ -78,3 +80,58 @@ def test_edge_values_agree_everywhere(kind):
     assert rep.mismatches() == 0
     off.close()
     dev.close()
+
+
+@pytest.mark.parametrize("hp,t0", [((1e-3, 0.0, 0.0, 1e-8), 0),
+                                   ((0.0, 0.9, 0.95, 1e-8), 0),
+                                   ((1e-3, 0.9, 0.95, 1.0), 0),
+                                   ((1e-3, 0.9, 0.95, 1e-30), 0),
+                                   ((1e-3, 0.9, 0.999, 1e-8), 999_999)])
+@pytest.mark.parametrize("scheme", [zs.ZERO_SCHEME_Z2, zs.ZERO_SCHEME_Z3])
+def test_hyperparameter_edges_on_the_gpu(scheme, hp, t0):
+    """No momentum (beta = 0), lr = 0, eps above and far below every |g|, and
+    a step counter so large that beta^t underflows: the kernels against the
+    oracle and bit for bit against the host update, which repeats their
+    arithmetic.  The state is restored at step t0 through zero_set_state."""
+    n, Wr = 20_011, 8
+    rng = np.random.default_rng(int(1e6 * hp[0]) + t0)
+    theta0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    units = [n] if scheme != zs.ZERO_SCHEME_Z3 else [7_001, 13_010]
+    st = zs.ZeroStep(scheme, Wr, units, "bf16", theta0=torch.from_numpy(theta0), device="cuda",
+                     stream=torch.cuda.Stream())
+    idx = st.real_index()
+    if t0:
+        zs.zero_set_state(st.ctx, st.master.clone(), st.m.clone(), st.v.clone(), t0)
+    orc = z.SingleReplica(theta0.copy(), "bf16")
+    orc.t = t0
+    host = [torch.from_numpy(theta0.copy()), torch.zeros(n), torch.zeros(n)]
+    host16 = torch.zeros(n, dtype=torch.int16)
+    grads = st.new_grad_buffers()
+    for t in range(t0 + 1, t0 + 4):
+        per_rank = (rng.standard_normal((Wr, n)) * 1e-3).astype(np.float32)
+        per_rank[:, rng.random(n) < 0.01] = 0.0
+        draws = [torch.from_numpy(x).to(torch.bfloat16) for x in per_rank]
+        torch.cuda.synchronize()
+        for g, d in zip(grads, draws):
+            g.zero_()
+            g[idx] = d.cuda()
+        torch.cuda.synchronize()
+        st.step(grads, *hp, t)
+        # the rank mean as the kernel forms it: fp32 additions in rank order, then / W (exact for W = 8)
+        acc = draws[0].float()
+        for d in draws[1:]:
+            acc = acc + d.float()
+        mean = acc / Wr
+        zs.zero_adam_host(n, mean, *host, host16, zs.ZERO_BF16, *hp, t, Wr, 2)
+        orc.step([wk.to_numpy16(d) for d in draws], *hp)
+    st.sync()
+    got = [st.master[idx].cpu(), st.m[idx].cpu(), st.v[idx].cpu()]
+    for a, b, what in zip(got, host, ("master", "m", "v")):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), what
+    assert_f32_close(got[0].numpy(), orc.master, "master")
+    assert_f32_close(got[1].numpy(), orc.m, "m")
+    assert_f32_close(got[2].numpy(), orc.v, "v")
+    assert torch.equal(st.working_copy()[idx].cpu().view(torch.int16), host16)
+    if hp[0] == 0.0:
+        assert np.array_equal(got[0].numpy().view(np.uint32), theta0.view(np.uint32))
+    st.close()

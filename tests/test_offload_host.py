@@ -79,6 +79,46 @@ def _err(fn, *args):
     return e.value.code
 
 
+@pytest.mark.parametrize("hp,t0", [((1e-3, 0.0, 0.0, 1e-8), 0),        # no momentum: m = g, v = g^2
+                                   ((0.0, 0.9, 0.95, 1e-8), 0),        # lr 0: theta stays, m and v move
+                                   ((1e-3, 0.9, 0.95, 1.0), 0),        # eps above every |g|
+                                   ((1e-3, 0.9, 0.95, 1e-30), 0),      # eps far below every |g|
+                                   ((1e-3, 0.9, 0.999, 1e-8), 999_999)])   # beta^t underflows: no bias correction
+def test_host_adam_hyperparameter_edges_match_the_oracle(zlib, hp, t0):
+    """The update at the edges of its hyper-parameters, with about 1% zero
+    gradients, against the oracle; the same fp32 arithmetic as the kernels."""
+    rng = np.random.default_rng(int(1e6 * hp[0]) + t0)
+    n = 20_011
+    theta0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    th, m, v = torch.from_numpy(theta0.copy()), torch.zeros(n), torch.zeros(n)
+    out = torch.zeros(n, dtype=torch.int16)
+    o = z.SingleReplica(theta0.copy(), "bf16")
+    for t in range(t0 + 1, t0 + 4):
+        g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        g[rng.random(n) < 0.01] = 0.0
+        zs.zero_adam_host(n, torch.from_numpy(g), th, m, v, out, zs.ZERO_BF16, *hp, t, 8, 2)
+        z.adam_update(o.master, o.m, o.v, g.astype(np.float64), *hp, t)
+    assert_f32_close(th.numpy(), o.master, "master")
+    assert_f32_close(m.numpy(), o.m, "m")
+    assert_f32_close(v.numpy(), o.v, "v")
+    if hp[0] == 0.0:
+        assert np.array_equal(th.numpy().view(np.uint32), theta0.view(np.uint32))
+
+
+def test_host_adam_refuses_what_fp32_cannot_carry(zlib):
+    """eps that rounds to 0 in fp32, or beyond its range, and a step size
+    lr / (1 - beta1^t) beyond it, are refused before any arithmetic."""
+    x = torch.zeros(8)
+    o = torch.zeros(8, dtype=torch.int16)
+    assert _err(zs.zero_adam_host, 8, x, x, x, x, o, 0, 1e-3, 0.9, 0.95, 1e-50, 1) == zs.ZERO_E_ARG
+    assert "eps" in zs.zero_last_error()
+    assert _err(zs.zero_adam_host, 8, x, x, x, x, o, 0, 1e-3, 0.9, 0.95, 1e39, 1) == zs.ZERO_E_ARG
+    assert _err(zs.zero_adam_host, 8, x, x, x, x, o, 0, 1e38, 0.9, 0.95, 1e-8, 1) == zs.ZERO_E_ARG  # 1e38 / 0.1
+    assert "overflows" in zs.zero_last_error()
+    zs.zero_adam_host(8, x, x, x, x, o, 0, 1e38, 0.9, 0.95, 1e-8, 100)   # 1 - 0.9^100 is about 1: fits
+    zs.zero_adam_host(8, x, x, x, x, o, 0, 1e-3, 0.9, 0.95, 1e-44, 1)    # a subnormal fp32 eps is still > 0
+
+
 def test_host_adam_checks(zlib):
     x = torch.zeros(8)
     o = torch.zeros(8, dtype=torch.int16)

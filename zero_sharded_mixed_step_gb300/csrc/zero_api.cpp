@@ -130,6 +130,15 @@ int check_hyper(double lr, double b1, double b2, double eps, int64_t t) {
   if (!(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1)) return fail(ZERO_E_ARG, "betas must lie in [0, 1)");
   if (!std::isfinite(eps) || !(eps > 0)) return fail(ZERO_E_ARG, "eps must be finite and > 0");
   if (t < 1) return fail(ZERO_E_STATE, "the step counter starts at 1 (got %lld)", (long long)t);
+  // The update runs in fp32: eps must stay a positive fp32 value (an eps that
+  // rounds to 0 makes 0 / 0 of every element without gradient history), and
+  // the step size lr / (1 - beta1^t) a finite one (inf times a zero m is NaN).
+  const float eps32 = static_cast<float>(eps);
+  if (!(eps32 > 0) || !std::isfinite(eps32))
+    return fail(ZERO_E_ARG, "eps %g is not a positive finite fp32 value", eps);
+  const double step_size = lr / (1.0 - std::pow(b1, static_cast<double>(t)));
+  if (!std::isfinite(static_cast<float>(step_size)))
+    return fail(ZERO_E_ARG, "lr / (1 - beta1^t) = %g overflows fp32", step_size);
   return ZERO_OK;
 }
 
