@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import zero_sharded_mixed_step_gb300 as zs
@@ -68,6 +69,27 @@ def test_layout_equals_oracle(zlib, units, W):
         assert s["shard_store"] == L.S_total and s["unit_buf"] == max(x * W for x in L.S) and s["p16"] == 0
     else:
         assert s["p16"] == L.n_pad and s["shard_store"] == 0
+
+
+def test_random_layouts_and_accounting_equal_the_oracle(zlib):
+    """300 seeded random configurations: unit lists of 1 to 40 units (empty
+    ones included) and W from 1 to 64 for the layout; n up to 10^13 for the
+    closed-form accounting of every scheme."""
+    rng = np.random.default_rng(2024)
+    for _ in range(300):
+        W = int(rng.integers(1, 65))
+        units = [int(x) for x in rng.integers(0, 10_000_000, int(rng.integers(1, 41)))]
+        units = [0 if rng.random() < 0.1 else u for u in units]
+        L = z.Layout(W, units)
+        off, shard, off16 = zs.zero_layout(W, units)
+        assert (off, shard, off16) == (L.off, L.S, L.off16), (W, units)
+        n = int(rng.integers(0, 10**13))
+        gathered = int(rng.integers(0, 10**9))
+        for scheme in (0, 1, 2, 3):
+            assert zs.zero_bytes_per_rank(scheme, n, W) == z.bytes_per_rank(scheme, n, W), (scheme, n, W)
+            assert zs.zero_bytes_per_rank(scheme, n, W, zs.ZERO_PEAK, gathered) == \
+                z.peak_bytes_per_rank(scheme, n, W, gathered), (scheme, n, W, gathered)
+            assert zs.zero_comm_bytes_closed_form(scheme, n, W) == z.comm_bytes_closed_form(scheme, n, W)
 
 
 def _err(fn, *args, **kw):
