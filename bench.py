@@ -576,6 +576,7 @@ def link_probe(h2d_pairs, d2h_pairs, stream):
     import torch
     h2d = sum(src.numel() * src.element_size() for _, src in h2d_pairs)
     d2h = sum(src.numel() * src.element_size() for _, src in d2h_pairs)
+    back = torch.cuda.Stream(stream.device)
     with torch.cuda.stream(stream):
         stream.synchronize()
         t0 = time.perf_counter()
@@ -587,9 +588,20 @@ def link_probe(h2d_pairs, d2h_pairs, stream):
             dst.copy_(src, non_blocking=True)
         stream.synchronize()
         t2 = time.perf_counter()
+        # both directions at once, as in a step: the link shares its rate between them
+        for dst, src in h2d_pairs:
+            dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(back):
+            for dst, src in d2h_pairs:
+                dst.copy_(src, non_blocking=True)
+        stream.synchronize()
+        back.synchronize()
+        t3 = time.perf_counter()
     return {"h2d_gbs": h2d / (t1 - t0) / 1e9, "d2h_gbs": d2h / (t2 - t1) / 1e9, "floor_ms": 1e3 * (t1 - t0),
+            "both_directions_ms": 1e3 * (t3 - t2),
             "note": "plain copies of the step's bytes timed just before the end-to-end steps; "
-                    "floor = the step's gradients carried in at that rate"}
+                    "floor = the step's gradients carried in at that rate; both_directions = the "
+                    "gradients in and the read-back out issued together on two streams"}
 
 
 class StepMarks:
