@@ -81,3 +81,59 @@ def test_two_stream_schedule_under_random_delays(seed):
     assert torch.equal(st.working_copy(), ref.working_copy())
     st.close()
     ref.close()
+
+
+@pytest.mark.parametrize("scheme,units,W,chunk", [(zs.ZERO_SCHEME_Z2, [1_000_003], 8, 100_000),
+                                                  (zs.ZERO_SCHEME_Z3, [262_147, 5, 500_000, 17], 5, 0)])
+def test_host_fed_ring_under_random_delays(scheme, units, W, chunk):
+    """zero_step_host's three streams, each held back by a random bounded
+    sleep before every step, with three steps enqueued back to back and no
+    host synchronisation between them: the two-slot staging ring, the
+    read-back of each step and the next step's update of the same values
+    must keep their order.  Each step's read-back must equal the working
+    copy the device step had after that step; the final state must equal it
+    bit for bit."""
+    n = sum(units)
+    wl = wk.scaled(wk.GPT2_SMALL, unit_sizes=units if scheme == zs.ZERO_SCHEME_Z3 else None, n=n, W=W, steps=3,
+                   name="host_races")
+    theta0 = wk.draw_theta0(wl, "cuda")
+    s_up, sh, sd = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    a = zs.ZeroStep(scheme, W, units, "bf16", theta0=theta0)
+    b = zs.ZeroStep(scheme, W, units, "bf16", theta0=theta0, stream=s_up)
+    need = zs.zero_host_staging_bytes(scheme, W, units, chunk)
+    staging = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out_elems = b.n_pad if scheme != zs.ZERO_SCHEME_Z3 else W * b.sizes["shard_store"]
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    src = wk.GradSource(wl, "bf16", "cuda")
+
+    def result(st):
+        return (st.p16 if scheme != zs.ZERO_SCHEME_Z3 else torch.cat(list(st.shard16))).cpu()
+
+    host_grads, host_out, want = [], [], []
+    for t in range(1, wl.steps + 1):
+        dev = []
+        for d in src.step(t):
+            g = torch.zeros(a.n_pad, dtype=a.grad_torch_dtype, device="cuda")
+            a.place_(g, d)
+            dev.append(g)
+        a.step(dev, *hp, t)
+        torch.cuda.synchronize()
+        host_grads.append([g.cpu().pin_memory() for g in dev])
+        host_out.append(torch.zeros(out_elems, dtype=b.work_torch_dtype).pin_memory())
+        want.append(result(a))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(len(units))
+    for t in range(1, wl.steps + 1):
+        for s in (s_up, sh, sd):
+            with torch.cuda.stream(s):
+                torch.cuda._sleep(int(rng.integers(0, 400_000)))   # bounded: at most ~0.2 ms at 2 GHz
+        zs.zero_step_host(b.ctx, scheme, W, n, host_grads[t - 1], host_out[t - 1], staging, need, chunk, *hp, t,
+                          sh, sd)
+    b.sync(timeout_ms=60_000)
+    torch.cuda.synchronize()
+    for t in range(1, wl.steps + 1):
+        assert torch.equal(host_out[t - 1].view(torch.int16), want[t - 1].view(torch.int16)), f"read-back of step {t}"
+    for x, y, what in ((a.master, b.master, "master"), (a.m, b.m, "m"), (a.v, b.v, "v")):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32)), what
+    a.close()
+    b.close()
