@@ -367,3 +367,14 @@ def test_binding_signatures_match_the_header():
             raw_ok = "*" in p and a is ctypes.c_void_p
             assert raw_ok or _ctype_of(p) == a, (name, p, a)
         assert _ctype_of(ret + " x" if not ret.endswith("*") else ret) == res, (name, ret, res)
+
+
+def test_strided_tensors_are_refused_by_the_binding(zlib):
+    """The library reads dense vectors from a base address: a strided view
+    would be read as the wrong elements, so the binding refuses it."""
+    import torch
+    x = torch.zeros(64)
+    with pytest.raises(ValueError):
+        zs.zero_adam_host(32, x[::2], x[:32], x[:32], x[:32], torch.zeros(32, dtype=torch.int16), 0,
+                          1e-3, 0.9, 0.95, 1e-8, 1)
+    assert zs._ptr(x[8:16]) == x.data_ptr() + 32       # a contiguous slice passes with its own address

@@ -127,6 +127,9 @@ def _ptr(x):
     if x is None:
         return None
     if hasattr(x, "data_ptr"):
+        # the library reads and writes dense vectors from this address
+        if hasattr(x, "is_contiguous") and not x.is_contiguous():
+            raise ValueError("a tensor passed to the library must be contiguous")
         return x.data_ptr()
     return int(x)
 
