@@ -2,7 +2,10 @@
 seeded inputs and compare it with the CPU oracle on the same draws.
 
 Tolerances: fp32 master, m and v within |a - b| <= 1e-5 |b| + 1e-7 of the
-oracle; accounting integers exact.  The 16-bit working copy is checked two
+oracle (the stated gate), and also within 1e-5 |b| + 1e-6 max|b| per array
+(the same relative bound with the absolute floor scaled to the array: at
+these gradient scales v is ~1e-10 and m ~1e-5, where a fixed 1e-7 floor
+would accept anything); accounting integers exact.  The 16-bit working copy is checked two
 ways: it must be exactly the round-to-nearest-even of the GPU's own master
 (the recast the pages define), and within 1 unit in the last place of the
 oracle's rounding of some master value inside the fp32 tolerance band of the
@@ -36,11 +39,49 @@ def assert_f32_close(got: np.ndarray, ref: np.ndarray, what: str):
 
 
 def diagnostic_error(got: np.ndarray, ref: np.ndarray) -> float:
-    """Worst error against 1e-5 |ref| + 1e-6 max|ref| (reported, not gated)."""
+    """Worst error against 1e-5 |ref| + 1e-6 max|ref| (1 = at the bound)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     floor = 1e-6 * (np.abs(ref).max() if ref.size else 0.0) + 1e-30
     return float(np.max(np.abs(got - ref) / (RTOL * np.abs(ref) + floor))) if ref.size else 0.0
+
+
+def assert_f32_parity(got: np.ndarray, ref: np.ndarray, what: str) -> float:
+    """Both fp32 gates: the stated tolerance, and the array-scaled one
+    (diagnostic_error <= 1).  Returns the diagnostic error."""
+    assert_f32_close(got, ref, what)
+    d = diagnostic_error(got, ref)
+    assert d <= 1.0, f"{what}: error {d:.3g} x (1e-5 |ref| + 1e-6 max|ref|)"
+    return d
+
+
+def band_width_ulps(ref_master: np.ndarray, dtype: str) -> np.ndarray:
+    """16-bit ulps between the roundings of the two ends of each element's
+    fp32 tolerance band: <= 1 where the band reading of the 1-ulp bound is
+    the plain 1-ulp bound."""
+    ref = np.asarray(ref_master, np.float64)
+    tol = RTOL * np.abs(ref) + ATOL
+    lo = _ordered16(z.bits16(z.cast16((ref - tol).astype(np.float32), dtype), dtype))
+    hi = _ordered16(z.bits16(z.cast16((ref + tol).astype(np.float32), dtype), dtype))
+    return hi - lo
+
+
+def assert_strict_ulp16(got_bits: np.ndarray, ref_master: np.ndarray, ref_bits: np.ndarray, dtype: str,
+                        what: str) -> tuple[int, int]:
+    """The plain 1-ulp bound against the oracle's own rounding, asserted at
+    every element whose tolerance band spans at most one 16-bit ulp; the
+    elements where it spans more (masters cancelled to ~1e-9, where fp32
+    and fp64 round to different tiny values) are counted, not gated.
+    Returns (misses where gated (always 0), misses where not gated)."""
+    miss = z.ulp_distance16(got_bits, ref_bits) > 1
+    gated = band_width_ulps(ref_master, dtype) <= 1
+    bad = miss & gated
+    if bad.any():
+        i = int(np.argmax(bad))
+        raise AssertionError(f"{what}: {int(bad.sum())} 16-bit values more than 1 ulp from the oracle's rounding "
+                             f"where the tolerance band is within one ulp; first at {i}: {int(got_bits[i]):#06x} "
+                             f"vs {int(ref_bits[i]):#06x}")
+    return 0, int((miss & ~gated).sum())
 
 
 def assert_ulp16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str, max_ulp: int = 1):
@@ -140,14 +181,15 @@ class Run:
         th, m, v, p16 = self.gpu_state()
         o = self.oracle
         tag = f"{self.wl.name} scheme {self.scheme} {self.dtype} t={self.t} {what}"
-        assert_f32_close(th, o.master, f"{tag} master")
-        assert_f32_close(m, o.m, f"{tag} m")
-        assert_f32_close(v, o.v, f"{tag} v")
+        errs = dict(master=assert_f32_parity(th, o.master, f"{tag} master"),
+                    m=assert_f32_parity(m, o.m, f"{tag} m"),
+                    v=assert_f32_parity(v, o.v, f"{tag} v"))
         assert_16bit_band(p16, o.master, self.work_dtype, f"{tag} 16-bit copy")
         own = bits_of(self.zs.master[self.sample_flat].to(self.zs.work_torch_dtype))
         assert np.array_equal(p16, own), f"{tag}: 16-bit copy is not the RNE of the GPU master"
-        self.strict_ulp_misses = int((z.ulp_distance16(p16, o.working_copy()) > 1).sum())
-        return dict(master=diagnostic_error(th, o.master), m=diagnostic_error(m, o.m), v=diagnostic_error(v, o.v))
+        _, self.strict_ulp_misses = assert_strict_ulp16(p16, o.master, o.working_copy(), self.work_dtype,
+                                                        f"{tag} 16-bit copy")
+        return errs
 
     def padding_is_zero(self):
         n_pad = self.zs.n_pad

@@ -427,13 +427,62 @@ def check_zero3_schedule(z):
             assert np.array_equal(bits, cast_before[lo:hi]), (t, ph, u)
         assert o.live == 0
     assert o.peak_live_elems == max(s * W for s in L.S)
-    assert z.peak_bytes_per_rank(z.ZERO3, L.n, W, o.peak_live_elems, S=L.S_total) == \
-        16 * L.S_total + 2 * o.peak_live_elems
     assert o.comm_bytes() == steps * 3 * sum((W - 1) * 2 * s for s in L.S)
+
+
+def load_peak_pins():
+    rows = []
+    with open(os.path.join(GOLDEN, "peak_pins.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            pid, where, psi, N, S, gathered, peak, elems, printed = [x.strip() for x in line.split("|")]
+            rows.append(dict(id=pid, where=where, psi=int(psi), N=int(N), S=int(S), gathered=gathered,
+                             peak=int(peak), elems=int(elems), printed=printed))
+    return rows
+
+
+def check_peak_bytes(z):
+    """Peak bytes of a ZeRO-3 rank against what the pages state: "own shard
+    plus one borrowed layer" ("ZeRO, annotated", section 7, stage 3 step by
+    step) and 2/64 of the parameters at peak on 64 devices ("One Poem
+    Suffices: ZeRO", section 4.1.4).  The 64-device case runs the oracle's
+    ZeRO-3 schedule on the scaled model and takes the gathered values from
+    what the schedule held live, not from the row."""
+    rows = load_peak_pins()
+    assert len(rows) == 3
+    for row in rows:
+        N, S, psi = row["N"], row["S"], row["psi"]
+        if row["gathered"] == "schedule":
+            block = psi // 192
+            units = [3 * block] * 64
+            theta0 = np.linspace(-1.0, 1.0, psi, dtype=np.float32)
+            o = z.ZeRO3(N, theta0, "fp16", units)
+            assert o.layout.S_total == S, (row["id"], o.layout.S_total)
+            grads = [np.full(psi, 0.25 * (r + 1), np.float16) for r in range(N)]
+            o.step([z.place(g, o.layout) for g in grads], 1e-3, 0.9, 0.999, 1e-8)
+            gathered = o.peak_live_elems
+            assert o.live == 0
+        else:
+            gathered = int(row["gathered"])
+        peak = z.peak_bytes_per_rank(z.ZERO3, psi, N, gathered, S=S)
+        assert peak == row["peak"], (row["id"], peak, row["peak"])
+        # the parameter part of the peak: the rank's own 16-bit shard plus the gathered values
+        param_bytes = peak - (z.bytes_per_rank(z.ZERO3, psi, N, S) - z.B_P16 * S)
+        assert param_bytes == z.B_P16 * row["elems"], (row["id"], param_bytes)
+        if row["printed"].startswith("2/64"):
+            assert 64 * row["elems"] == 2 * psi, row["id"]
+        else:                                  # own shard plus one borrowed layer of one shard
+            assert row["elems"] == 2 * S and gathered == S, row["id"]
+        # the other schemes gather nothing: their peak is what they hold
+        for scheme in (z.DP, z.ZERO1, z.ZERO2):
+            assert z.peak_bytes_per_rank(scheme, psi, N, gathered, S=S) == z.bytes_per_rank(scheme, psi, N, S)
 
 
 ALL_CHECKS = [
     check_accounting, check_padded_state_bytes, check_traffic_from_events, check_layer_unit_traffic,
     check_scheme_invariance, check_first_step, check_vs_torch_adam, check_brute_force,
     check_padding_stays_zero, check_rounding, check_zero_check_example, check_zero3_schedule,
+    check_peak_bytes,
 ]

@@ -9,7 +9,7 @@ import torch
 import zero_sharded_mixed_step_gb300 as zs
 import workloads as wk
 from oracle import zero_oracle as z
-from tests.gpu_harness import assert_16bit_band, assert_f32_close, bits_of, sample_real_indices
+from tests.gpu_harness import assert_16bit_band, assert_f32_parity, bits_of, sample_real_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -28,9 +28,9 @@ def _fill(bufs, draws, n):
 
 def _check_replica(rep, r, master, m, v, dtype, tag, idx=None):
     sel = (lambda x: x) if idx is None else (lambda x: x[idx])
-    assert_f32_close(sel(rep.master[r]).cpu().numpy(), master, f"{tag} replica {r} master")
-    assert_f32_close(sel(rep.m[r]).cpu().numpy(), m, f"{tag} replica {r} m")
-    assert_f32_close(sel(rep.v[r]).cpu().numpy(), v, f"{tag} replica {r} v")
+    assert_f32_parity(sel(rep.master[r]).cpu().numpy(), master, f"{tag} replica {r} master")
+    assert_f32_parity(sel(rep.m[r]).cpu().numpy(), m, f"{tag} replica {r} m")
+    assert_f32_parity(sel(rep.v[r]).cpu().numpy(), v, f"{tag} replica {r} v")
     p16 = bits_of(sel(rep.p16[r]))
     assert_16bit_band(p16, master, dtype, f"{tag} replica {r} 16-bit copy")
     own = bits_of(sel(rep.master[r]).to(rep.work_torch_dtype))

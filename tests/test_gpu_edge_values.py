@@ -12,7 +12,7 @@ import torch
 import workloads as wk
 import zero_sharded_mixed_step_gb300 as zs
 from oracle import zero_oracle as z
-from tests.gpu_harness import assert_16bit_band, assert_f32_close, bits_of
+from tests.gpu_harness import assert_16bit_band, assert_f32_parity, bits_of
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +59,7 @@ def test_edge_values_agree_everywhere(kind):
         orc.step([d.numpy() for d in draws], *HP)
         torch.cuda.synchronize()
         th = dev.master[:n].cpu().numpy()
-        assert_f32_close(th, orc.master, f"{kind} t={t} master")
+        assert_f32_parity(th, orc.master, f"{kind} t={t} master")
         p16 = bits_of(dev.p16[:n])
         assert_16bit_band(p16, orc.master, "fp16", f"{kind} t={t} working copy")
         assert np.array_equal(p16, bits_of(dev.master[:n].to(torch.float16)))
@@ -128,9 +128,9 @@ def test_hyperparameter_edges_on_the_gpu(scheme, hp, t0):
     got = [st.master[idx].cpu(), st.m[idx].cpu(), st.v[idx].cpu()]
     for a, b, what in zip(got, host, ("master", "m", "v")):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32)), what
-    assert_f32_close(got[0].numpy(), orc.master, "master")
-    assert_f32_close(got[1].numpy(), orc.m, "m")
-    assert_f32_close(got[2].numpy(), orc.v, "v")
+    assert_f32_parity(got[0].numpy(), orc.master, "master")
+    assert_f32_parity(got[1].numpy(), orc.m, "m")
+    assert_f32_parity(got[2].numpy(), orc.v, "v")
     assert torch.equal(st.working_copy()[idx].cpu().view(torch.int16), host16)
     if hp[0] == 0.0:
         assert np.array_equal(got[0].numpy().view(np.uint32), theta0.view(np.uint32))

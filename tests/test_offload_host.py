@@ -9,7 +9,7 @@ import torch
 import zero_sharded_mixed_step_gb300 as zs
 from oracle import zero_oracle as z
 
-from tests.gpu_harness import assert_f32_close
+from tests.gpu_harness import assert_f32_parity
 
 
 def _run(g_steps, theta0, dtype, threads, hp=(1e-3, 0.9, 0.95, 1e-8)):
@@ -36,9 +36,9 @@ def test_host_adam_matches_the_oracle(zlib, dtype):
     o = z.SingleReplica(theta0.copy(), dtype)
     for t, g in enumerate(g_steps, start=1):
         z.adam_update(o.master, o.m, o.v, g.astype(np.float64), 1e-3, 0.9, 0.95, 1e-8, t)
-    assert_f32_close(th, o.master, "master")
-    assert_f32_close(m, o.m, "m")
-    assert_f32_close(v, o.v, "v")
+    assert_f32_parity(th, o.master, "master")
+    assert_f32_parity(m, o.m, "m")
+    assert_f32_parity(v, o.v, "v")
     # the 16-bit copy is exactly the round-to-nearest-even of the host master
     assert np.array_equal(out, z.bits16(z.cast16(th, dtype), dtype))
 
@@ -98,9 +98,9 @@ def test_host_adam_hyperparameter_edges_match_the_oracle(zlib, hp, t0):
         g[rng.random(n) < 0.01] = 0.0
         zs.zero_adam_host(n, torch.from_numpy(g), th, m, v, out, zs.ZERO_BF16, *hp, t, 8, 2)
         z.adam_update(o.master, o.m, o.v, g.astype(np.float64), *hp, t)
-    assert_f32_close(th.numpy(), o.master, "master")
-    assert_f32_close(m.numpy(), o.m, "m")
-    assert_f32_close(v.numpy(), o.v, "v")
+    assert_f32_parity(th.numpy(), o.master, "master")
+    assert_f32_parity(m.numpy(), o.m, "m")
+    assert_f32_parity(v.numpy(), o.v, "v")
     if hp[0] == 0.0:
         assert np.array_equal(th.numpy().view(np.uint32), theta0.view(np.uint32))
 

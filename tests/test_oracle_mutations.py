@@ -119,6 +119,11 @@ MUTANTS = {
     "z3_two_collectives": ("comm_bytes_closed_form",
                            lambda s, n, W, S=None: 2 * z.ring_bytes_per_rank(W, S or z.shard_size(n, W))),
     "ring_sends_W_chunks": ("ring_bytes_per_rank", lambda W, s, elem_bytes=2: W * s * elem_bytes),
+    "peak_gathers_fp32": ("peak_bytes_per_rank",
+                          lambda sc, n, W, g=0, S=None: z.bytes_per_rank(sc, n, W, S) + (4 * g if sc == z.ZERO3 else 0)),
+    "peak_without_gathered": ("peak_bytes_per_rank", lambda sc, n, W, g=0, S=None: z.bytes_per_rank(sc, n, W, S)),
+    "peak_gathers_in_every_scheme": ("peak_bytes_per_rank",
+                                     lambda sc, n, W, g=0, S=None: z.bytes_per_rank(sc, n, W, S) + 2 * g),
 }
 
 CLASS_MUTANTS = {
