@@ -378,3 +378,28 @@ def test_strided_tensors_are_refused_by_the_binding(zlib):
         zs.zero_adam_host(32, x[::2], x[:32], x[:32], x[:32], torch.zeros(32, dtype=torch.int16), 0,
                           1e-3, 0.9, 0.95, 1e-8, 1)
     assert zs._ptr(x[8:16]) == x.data_ptr() + 32       # a contiguous slice passes with its own address
+
+
+def test_static_z3_step_checks_before_any_launch(zlib):
+    """The ZeRO-3 step without allocations refuses units beyond its fixed
+    gather array, before any CUDA call and before any arithmetic on the
+    size that could overflow; and refuses the usual bad arguments."""
+    hp = (1e-3, 0.9, 0.95, 1e-8)
+
+    def call(W, units, th=None, s16=None, g=None, t=1):
+        th = fake(1) if th is None else th
+        s16 = [fake(10 + r) for r in range(W)] if s16 is None else s16
+        g = [fake(40 + r) for r in range(W)] if g is None else g
+        return _err(zs.zero_step_z3_static, W, units, 1, 1, th, fake(2), fake(3), s16, g, *hp, t)
+
+    for W, units in ((1, [8_388_609]), (3, [8_388_607]), (1, [2**63 - 1]), (5, [2**63 - 2]), (2, [17, 2**62]),
+                     (7, [8_388_605])):
+        assert call(W, units) == zs.ZERO_E_ARG, (W, units)
+        assert "static gather buffer" in zs.zero_last_error()
+    assert call(0, [10]) == zs.ZERO_E_ARG
+    assert call(65, [10]) == zs.ZERO_E_ARG
+    assert call(2, [-1]) == zs.ZERO_E_ARG
+    assert call(2, [10], t=0) == zs.ZERO_E_STATE
+    assert call(2, [10], th=fake(1) + 16) == zs.ZERO_E_ALIGN
+    assert call(2, [10], s16=[fake(10), fake(11) + 2]) == zs.ZERO_E_ALIGN
+    assert call(2, [10], g=[fake(40), None]) == zs.ZERO_E_ARG

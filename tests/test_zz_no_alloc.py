@@ -7,8 +7,8 @@ into a fixed array that belongs to the library.  Here the caller owns only
 its state (master, m, v, the ranks' 16-bit shard stores, the gradients);
 two calls in a row must leave that state where two zero_step calls leave
 it, within the parity tolerances, and the hook must see every gathered unit
-in the library's array.  This file is collected last and needs nothing
-from the tests before it.
+in the library's array; the same must hold across a cudaDeviceReset.  This
+file is collected last and needs nothing from the tests before it.
 """
 
 import numpy as np
@@ -44,7 +44,10 @@ def _caller_state(ref: zs.ZeroStep):
     return master, m, v, shards
 
 
-def test_static_scratch_step_matches_zero_step():
+@pytest.mark.parametrize("with_hook", [True, False], ids=["hook", "no_hook"])
+def test_static_scratch_step_matches_zero_step(with_hook):
+    """With a hook every gather is a copy of its own; without one each
+    backward gather is done by the unit's update pass, as in zero_step."""
     from zero_sharded_mixed_step_gb300 import build
     build.build()
     wl = wk.scaled(wk.LAYER_UNITS, unit_sizes=UNITS, steps=2, name="static_scratch")
@@ -76,7 +79,7 @@ def test_static_scratch_step_matches_zero_step():
         seen.clear()
         ref.step(grads, *hp, t)
         zs.zero_step_z3_static(W, UNITS, zs.ZERO_BF16, zs.ZERO_BF16, master, m, v, shards, grads, *hp, t,
-                               hook=hook)
+                               hook=hook if with_hook else None)
         torch.cuda.synchronize()
 
         # the state equals zero_step's, within the parity tolerances (and in fact bit for bit)
@@ -87,6 +90,8 @@ def test_static_scratch_step_matches_zero_step():
             gh.assert_16bit_band(gh.bits_of(shards[r]), _rank_master(ref, r), "bf16", f"t={t} shard store {r}")
             assert torch.equal(shards[r], ref.shard16[r]), f"t={t} shard store {r}"
 
+        if not with_hook:
+            continue
         # every unit gathered twice, in the ZeRO-3 order, into the library's one array
         U = len(UNITS)
         assert [(p, u) for p, u, _, _ in seen] == [(0, u) for u in range(U)] + [(1, u) for u in reversed(range(U))]
@@ -109,12 +114,47 @@ def _rank_master(ref: zs.ZeroStep, r: int) -> np.ndarray:
 def test_static_scratch_rejects_units_beyond_its_size():
     from zero_sharded_mixed_step_gb300 import build
     build.build()
-    big = [8_388_609]                                  # one value past the array, with W = 1
     x = torch.zeros(8_388_616, dtype=torch.float32, device="cuda")
     s16 = torch.zeros(8_388_616, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(zs.ZeroError) as e:
-        zs.zero_step_z3_static(1, big, zs.ZERO_BF16, zs.ZERO_BF16, x, x, x, [s16], [s16], 1e-3, 0.9, 0.95, 1e-8, 1)
-    assert e.value.code == zs.ZERO_E_ARG
-    assert "static gather buffer" in zs.zero_last_error()
+    # one value past the array (W = 1); one that only padding takes past it
+    # (W = 3); sizes whose padding would overflow int64 if computed first
+    for W, big in ((1, [8_388_609]), (3, [8_388_607]), (1, [2**63 - 1]), (5, [2**63 - 2]), (2, [17, 2**62])):
+        with pytest.raises(zs.ZeroError) as e:
+            zs.zero_step_z3_static(W, big, zs.ZERO_BF16, zs.ZERO_BF16, x, x, x, [s16] * W, [s16] * W,
+                                   1e-3, 0.9, 0.95, 1e-8, 1)
+        assert e.value.code == zs.ZERO_E_ARG, (W, big)
+        assert "static gather buffer" in zs.zero_last_error()
     torch.cuda.synchronize()
     assert bool((x == 0).all()) and bool((s16 == 0).all())   # nothing ran
+
+
+def test_static_scratch_step_survives_a_device_reset(tmp_path):
+    """A plain C client (tests/c_static_reset.c) runs the step without
+    allocations beside zero_step, resets the device with cudaDeviceReset
+    (freeing everything and unloading the library's device code, the
+    gather array with it), allocates again and runs both once more: the
+    same bits both times.  The array's address is looked up on each call,
+    so the call after the reset uses the reloaded array, not a stale
+    address.  Runs in its own process, so it neither needs nor disturbs
+    the state of this one."""
+    import os
+    import subprocess
+    from zero_sharded_mixed_step_gb300 import build
+    lib = build.build()
+    # the client and the library must share one CUDA runtime for the reset to reach the library
+    deps = subprocess.run(["ldd", lib], capture_output=True, text=True).stdout
+    assert "libcudart.so" in deps, deps
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    cuda = build.cuda_home()
+    libdir = os.path.dirname(lib)
+    exe = str(tmp_path / "c_static_reset")
+    res = subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(root, "include"), "-I",
+                          os.path.join(cuda, "include"), os.path.join(here, "c_static_reset.c"), "-o", exe,
+                          "-L", libdir, "-lzero_gb300", "-L", build.cudart_dir(), "-lcudart",
+                          f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{build.cudart_dir()}"],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "before and after cudaDeviceReset" in run.stdout

@@ -1,13 +1,17 @@
 """Build libzero_gb300.so in-tree for sm_103a with nvcc (no CMake).
 
 Translation units are compiled in parallel into ``_build/`` at the
-repository root and linked, with the CUDA runtime linked statically, into
-``zero_sharded_mixed_step_gb300/libzero_gb300.so``.  Run
+repository root and linked into ``zero_sharded_mixed_step_gb300/libzero_gb300.so``
+against the shared CUDA runtime (``libcudart.so``, found through the
+library's run path in the toolkit), so that the library, PyTorch and a C
+caller in one process share one runtime: device resets, errors and loaded
+modules are seen alike by all of them.  Run
 ``python -m zero_sharded_mixed_step_gb300.build`` or call ``build()``.
 """
 
 from __future__ import annotations
 
+import glob
 import os
 import subprocess
 import sys
@@ -31,10 +35,23 @@ HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "zero_conte
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
+def cuda_home() -> str:
+    return os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH") or "/usr/local/cuda"
+
+
 def nvcc() -> str:
-    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH") or "/usr/local/cuda"
-    path = os.path.join(home, "bin", "nvcc")
+    path = os.path.join(cuda_home(), "bin", "nvcc")
     return path if os.path.exists(path) else "nvcc"
+
+
+def cudart_dir() -> str:
+    """The toolkit directory holding libcudart.so (the library's run path)."""
+    home = cuda_home()
+    for cand in [os.path.join(home, "lib64"), os.path.join(home, "lib")] + \
+            sorted(glob.glob(os.path.join(home, "targets", "*", "lib"))):
+        if os.path.exists(os.path.join(cand, "libcudart.so")):
+            return cand
+    return os.path.join(home, "lib64")
 
 
 def _flags(ptxas_verbose: bool):
@@ -72,9 +89,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             jobs.append([nvcc()] + _flags(ptxas_verbose) + EXTRA_FLAGS.get(src, []) + ["-c", path, "-o", obj])
     with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as pool:
         list(pool.map(lambda c: _run(c, verbose or ptxas_verbose), jobs))
-    if force or jobs or _stale(LIB, objs):
+    if force or jobs or _stale(LIB, objs + [os.path.abspath(__file__)]):
         tmp = LIB + ".tmp"
-        _run([nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs, verbose)
+        _run([nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-Xlinker", "-rpath", "-Xlinker", cudart_dir(),
+                                 "-o", tmp] + objs, verbose)
         os.replace(tmp, LIB)
     return LIB
 

@@ -13,13 +13,20 @@
 // The array is a file-scope __device__ variable: every GPU on which the
 // library's code is loaded holds it until the process exits, and every
 // call shares it.  In host code its name is only a host-side stand-in, so
-// the device address is looked up once per device with cudaGetSymbolAddress
-// (with that device current) and that address is what the kernels receive.
+// each call looks up the device address with cudaGetSymbolAddress, with the
+// caller's device current, and hands that address to the kernels.  The
+// lookup is not cached: after cudaDeviceReset (or any teardown of the
+// device's context) the module is loaded again and the array may sit at
+// another address, and a cached one would then point at freed memory.
+//
+// The update runs the register kernel (ZERO_VARIANT_VECTOR), which has no
+// device-side waits.  The bulk-staged kernel bounds its waits and reports one
+// that runs out through a per-context counter, and this entry point has no
+// context to report it through.
 
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "zero_internal.h"
 #include "zero_step.h"
@@ -31,29 +38,17 @@ constexpr int64_t kStaticUnitElems = int64_t(8) << 20;
 
 static __device__ __align__(256) uint16_t g_static_unit[kStaticUnitElems];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_unit_addr[kMaxDevices] = {};
-
 // errors are reported through zero_last_error(), like every other entry point
 int set_error(int code, const char* msg) { return zero::record_error(code, msg); }
 
-// Device address of g_static_unit on the current device (looked up once per
-// device, the first time this entry point runs there).
+// Device address of g_static_unit on the current device, looked up on every
+// call (cheap next to the step, and never stale: see the top of the file).
 int unit_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error(ZERO_E_CUDA, cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return set_error(ZERO_E_ARG, "device index beyond the supported range");
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_unit_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_unit);
-    if (e != cudaSuccess || p == nullptr)
-      return set_error(ZERO_E_CUDA, e != cudaSuccess ? cudaGetErrorString(e) : "no device address for the scratch");
-    g_unit_addr[dev] = p;
-  }
-  *out = g_unit_addr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_static_unit);
+  if (e != cudaSuccess || p == nullptr)
+    return set_error(ZERO_E_CUDA, e != cudaSuccess ? cudaGetErrorString(e) : "no device address for the scratch");
+  *out = p;
   return ZERO_OK;
 }
 
@@ -76,11 +71,13 @@ extern "C" int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_s
   int64_t pos = 0, pos16 = 0;
   for (int64_t u = 0; u < n_units; ++u) {
     if (unit_sizes[u] < 0) return set_error(ZERO_E_ARG, "negative unit size");
-    const int64_t S = (unit_sizes[u] + W - 1) / W;
-    if (S * W > kStaticUnitElems)
+    // bounded before any arithmetic, so that padding cannot overflow
+    if (unit_sizes[u] > kStaticUnitElems ||
+        (unit_sizes[u] + W - 1) / W * W > kStaticUnitElems)
       return set_error(ZERO_E_ARG,
                        "a unit is larger than the static gather buffer (8,388,608 16-bit values after padding); "
                        "use zero_step with caller-allocated unit buffers");
+    const int64_t S = (unit_sizes[u] + W - 1) / W;
     pos += S * W;
     pos16 += S;
   }
@@ -105,26 +102,34 @@ extern "C" int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_s
   a.master = master;
   a.m = m;
   a.v = v;
-  a.variant = ZERO_VARIANT_AUTO;
+  a.variant = ZERO_VARIANT_VECTOR;   // no device-side waits (see the top of the file)
   a.coef = zero::adam_coef(lr, beta1, beta2, eps, t, W);
   int64_t launches = 0;
   // One stream and one buffer: each gather waits, in stream order, for the
-  // work that used the previous unit.
+  // work that used the previous unit.  Without a hook nothing runs between a
+  // unit's backward gather and its update, so the update pass does both: it
+  // copies each 16-bit value into the buffer before overwriting it.
   auto unit = [&](int64_t u, int64_t off, int64_t off16, int phase) -> int {
     const int64_t S = (unit_sizes[u] + W - 1) / W;
     if (S == 0) {
       if (hook) hook(user, phase, u, buf, stream);
       return ZERO_OK;
     }
-    zero::CopySeg segs[zero::kMaxCopySegs];
-    for (int r = 0; r < W; ++r)
-      segs[r] = {static_cast<const char*>(shard16[r]) + off16 * 2, static_cast<char*>(buf) + r * S * 2, S * 2};
-    cudaError_t e = zero::launch_copy(segs, W, s, &launches);
-    if (e != cudaSuccess) return set_error(ZERO_E_CUDA, cudaGetErrorString(e));
-    if (hook) hook(user, phase, u, buf, stream);
+    const bool fused_gather = phase == 1 && hook == nullptr;
+    cudaError_t e = cudaSuccess;
+    if (!fused_gather) {
+      zero::CopySeg segs[zero::kMaxCopySegs];
+      for (int r = 0; r < W; ++r)
+        segs[r] = {static_cast<const char*>(shard16[r]) + off16 * 2, static_cast<char*>(buf) + r * S * 2, S * 2};
+      e = zero::launch_copy(segs, W, s, &launches);
+      if (e != cudaSuccess) return set_error(ZERO_E_CUDA, cudaGetErrorString(e));
+      if (hook) hook(user, phase, u, buf, stream);
+    }
     if (phase == 1) {
       a.nseg = W;
-      for (int r = 0; r < W; ++r) a.segs[r] = {off + r * S, S, static_cast<char*>(shard16[r]) + off16 * 2, nullptr};
+      for (int r = 0; r < W; ++r)
+        a.segs[r] = {off + r * S, S, static_cast<char*>(shard16[r]) + off16 * 2,
+                     fused_gather ? static_cast<char*>(buf) + r * S * 2 : nullptr};
       e = zero::launch_fused_step(a, s, &launches);
       if (e != cudaSuccess) return set_error(ZERO_E_CUDA, cudaGetErrorString(e));
     }
