@@ -227,10 +227,12 @@ int zero_refresh_working_copy(zero_ctx* ctx);
  * next unit's gather overlaps the work on the current one (prefetch); with
  * none, everything runs in order on stream_update (there is no compute to
  * hide a gather behind): the forward pass gathers two units per launch, one
- * into each unit buffer, and each backward gather is done by the unit's
- * update pass, which copies the unit's 16-bit values into the unit buffer
- * before overwriting them.  At most two unit buffers are live.  Traffic:
- * 3 (W-1) S_u 2 bytes per unit.
+ * into each unit buffer - all the pairs in one launch when every unit has
+ * the same shard size, every buffer position receiving its units in unit
+ * order, so that the buffers end as after separate gathers - and each
+ * backward gather is done by the unit's update pass, which copies the
+ * unit's 16-bit values into the unit buffer before overwriting them.  At
+ * most two unit buffers are live.  Traffic: 3 (W-1) S_u 2 bytes per unit.
  * The step is ordered after earlier work on stream_update and all its work
  * is finished when work enqueued later on stream_update starts.
  */
@@ -490,10 +492,20 @@ int zero_mark_rank(zero_ctx* ctx, int rank, int available);
  * loaded until the process exits.  All calls share it and it keeps the last
  * call's contents (each gather overwrites what it reads, so nothing needs
  * clearing); calls whose work overlaps on the GPU race on it, so issue
- * them on one stream or otherwise serialise them.  The first call on a
- * device looks up the array's device address there (cudaGetSymbolAddress
- * with that device current); make that first call before any stream
- * capture.  Nothing here calls cudaMalloc, cudaFree or any other allocator.
+ * them on one stream or otherwise serialise them.  Every call looks up the
+ * array's device address on the current device (cudaGetSymbolAddress); the
+ * address is not kept between calls, so a call after cudaDeviceReset finds
+ * the array where the reloaded module put it.  The first call on a device
+ * also loads the library's device code there: make that first call before
+ * any stream capture.  Nothing here calls cudaMalloc, cudaFree or any other
+ * allocator.
+ *
+ * Without a hook, each unit's backward gather is done by its update pass
+ * (the pass copies each 16-bit value into the array before overwriting it),
+ * as zero_step does; with a hook the gather is a copy of its own, so that
+ * the hook sees the unit before it is updated.  The update runs the register
+ * kernel (ZERO_VARIANT_VECTOR): it has no device-side waits, so there is no
+ * timed-out wait that this context-free call would have to report.
  */
 int zero_step_z3_static(int W, int64_t n_units, const int64_t* unit_sizes, int grad_dtype, int work_dtype,
                         float* master, float* m, float* v, void* const* shard16, const void* const* grads,

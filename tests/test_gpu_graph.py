@@ -131,8 +131,9 @@ def test_full_zero3_workload_as_the_benchmark_runs_it():
     """The 24 x 50,331,648 workload on 8 ranks without a hook and with graph
     replay, the launch configuration the benchmark times: sampled parity with
     the oracle, bit-identical to ordinary launches on the same gradients,
-    traffic 6,341,787,648 B and U + U/2 launches per step (the forward
-    gathers two units per launch), two unit buffers at most."""
+    traffic 6,341,787,648 B and U + 1 launches per step (every unit has the
+    same size, so the forward gathers go in one launch), two unit buffers at
+    most."""
     wl = wk.scaled(wk.LAYER_UNITS, steps=3)
     U, S_u = len(wl.units()), wl.units()[0] // wl.W
     sample = gh.sample_real_indices(wl.n, wl.W, wl.units(), k=16384)
@@ -152,7 +153,7 @@ def test_full_zero3_workload_as_the_benchmark_runs_it():
         for a, b in zip(run.zs.shard16, plain.shard16):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
         assert zs.zero_comm_bytes_per_rank(run.zs.ctx) == wl.steps * 6_341_787_648
-        assert run.zs.stat(zs.ZERO_STAT_LAUNCHES) - launches0 == wl.steps * (U + (U + 1) // 2)
+        assert run.zs.stat(zs.ZERO_STAT_LAUNCHES) - launches0 == wl.steps * (U + 1)
         assert run.zs.stat(zs.ZERO_STAT_PEAK_LIVE_ELEMS) == 2 * S_u * wl.W
         assert run.zs.stat(zs.ZERO_STAT_LIVE_ELEMS) == 0
         plain.close()

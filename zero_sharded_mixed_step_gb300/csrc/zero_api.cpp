@@ -305,10 +305,13 @@ int poison_unit(zero_ctx* c, int64_t u, void* buf, cudaStream_t s) {
 // unit hook is registered; with no hook the only work on stream A is the
 // memory-bound update, and running the gathers beside it on GB300 measured
 // slower than running everything in order on stream A.  Without a hook the
-// forward gathers also go two units per launch (one into each buffer), and
-// each backward gather is done by its unit's update pass.  A unit counts as
-// live from its gather until its buffer is taken by a later gather (or the
-// step ends): at most two units are live.
+// forward gathers go in one launch when every unit has the same shard size
+// (zero::launch_gather_units: pair after pair of units, each buffer position
+// receiving its units in unit order), else two units per launch (one into
+// each buffer), and each
+// backward gather is done by its unit's update pass.  A unit counts as live
+// from its gather until its buffer is taken by a later gather (or the step
+// ends): at most two units are live.
 int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& coef) {
   int rc = ensure_cuda(c);
   if (rc) return rc;
@@ -360,7 +363,31 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
     used[b] = true;
     return ZERO_OK;
   };
-  if (c->hook == nullptr && 2 * c->W <= zero::kMaxCopySegs) {
+  bool equal_units = U > 0 && c->debug == 0;
+  for (int64_t u = 1; u < U && equal_units; ++u) equal_units = c->L.shard[u] == c->L.shard[0];
+  if (c->hook == nullptr && equal_units &&
+      zero::gather_units_applies(c->shard16.data(), c->W, c->ubuf, U, c->L.shard[0])) {
+    // Nothing runs between the forward gathers and every unit has the same
+    // shard size: all of them in one launch, pair after pair, each buffer
+    // position receiving its units in unit order (the buffers end as after
+    // the separate launches, and the same bytes move).
+    for (int64_t u = 0; u < U; ++u) {
+      const int b = static_cast<int>(seq++ & 1);
+      c->live_elems -= held[b];
+      held[b] = c->L.shard[u] * c->W;
+      live_add(c, held[b]);
+      count_gather(c, u);
+      used[b] = true;
+    }
+    Range range("zero3 forward units 0..%lld", static_cast<long long>(U - 1));
+    Bracket br{c, ZERO_KERNEL_GATHER, su};
+    if ((rc = br.open())) return rc;
+    const cudaError_t e = zero::launch_gather_units(c->shard16.data(), c->W, c->ubuf, U, c->L.shard[0], su,
+                                                    &c->launches);
+    if (e != cudaSuccess) return cuda_fail(e, "forward unit gathers launch");
+    touch(c, su);
+    if ((rc = br.close())) return rc;
+  } else if (c->hook == nullptr && 2 * c->W <= zero::kMaxCopySegs) {
     // Nothing runs between the forward gathers, so two units (one into each
     // buffer) go in one launch: the same copies in half the launches.
     for (int64_t u = 0; u < U; u += 2) {
@@ -398,8 +425,8 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
 
 // ---- ZeRO-3 steps replayed from a CUDA graph ----------------------------------------
 //
-// A ZeRO-3 step without a hook is a fixed sequence of 2 U launches on one
-// stream.  Captured once, it is replayed as one graph launch, which saves the
+// A ZeRO-3 step without a hook is a fixed sequence of launches on one stream
+// (the forward gathers, then one update per unit).  Captured once, it is replayed as one graph launch, which saves the
 // launch gaps between its kernels; only the fused kernels' Adam coefficients
 // and gradient pointers change from step to step, and they are set on the
 // graph's nodes before each replay.
@@ -462,7 +489,7 @@ int capture_zero3(zero_ctx* c, const void* const* grads, const zero::AdamCoef& c
     if (e1 != cudaSuccess || type != cudaGraphNodeTypeKernel) continue;
     cudaKernelNodeParams p;
     e1 = cudaGraphKernelNodeGetParams(nodes[k], &p);
-    if (e1 == cudaSuccess && p.func != zero::copy_kernel())
+    if (e1 == cudaSuccess && !zero::is_gather_kernel(p.func))
       c->graph_fused.emplace_back(nodes[k], *static_cast<const zero::FusedLaunch*>(p.kernelParams[0]));
   }
   if (e1 == cudaSuccess) e1 = cudaGraphInstantiate(&c->graph_exec, g, 0);

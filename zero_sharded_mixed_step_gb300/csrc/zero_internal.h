@@ -88,8 +88,18 @@ cudaError_t launch_fused_step(const FusedLaunch& a, cudaStream_t stream, int64_t
 // Gather: copy each segment's bytes (16-byte vectors where both ends allow).
 cudaError_t launch_copy(const CopySeg* segs, int nseg, cudaStream_t stream, int64_t* launches);
 
-// The gather kernel's device function (to tell its nodes apart in a captured graph).
-const void* copy_kernel();
+// Whether a kernel function is one of the gather kernels (to tell the nodes
+// of a captured graph apart from the fused kernels').
+bool is_gather_kernel(const void* fn);
+
+// Every forward gather of a ZeRO-3 step in one launch: unit u (of `units`,
+// each with shard size S, unit u's shard at u * S in every rank's store)
+// into bufs[u % 2].  Applies (gather_units_applies) when S * 2 is a multiple
+// of 32 bytes and the stores and buffers are 32-byte aligned; otherwise the
+// launch returns cudaErrorInvalidValue.
+bool gather_units_applies(const void* const* shard, int W, void* const* bufs, int64_t units, int64_t S);
+cudaError_t launch_gather_units(const void* const* shard, int W, void* const* bufs, int64_t units, int64_t S,
+                                cudaStream_t stream, int64_t* launches);
 
 // Fill count 16-bit values with `value` (debug poisoning of released units).
 cudaError_t launch_fill16(void* dst, int64_t count, uint16_t value, cudaStream_t stream, int64_t* launches);
