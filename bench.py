@@ -6,10 +6,14 @@ A step is one pass of the whole hot path over one batch of synthetic
 gradients: the mean reduce-scatter of W ranks' 16-bit gradients, Adam with
 bias correction on the fp32 master / m / v, the recast and gather of the
 16-bit working copy and, for ZeRO-3, the per-unit gather / release /
-re-gather schedule.  The default workload is the ZeRO-3 one (24 transformer-
-layer units of 50,331,648 parameters, 8 simulated ranks, bf16), the only one
-that passes through every stage; ``--workload`` selects the GPT-2-small
-(ZeRO-2) or GPT-2-1.5B (ZeRO-1) flat vectors instead.
+re-gather schedule.  The default workload is the largest that fits one GPU:
+a GPT-2-1.5B-sized flat vector (1,557,611,200 parameters, 16 simulated
+ranks, fp16, ZeRO-1).  The same process then times the other configurations
+on the device and reports them under ``also``: the ZeRO-3 layer-unit
+schedule (24 units of 50,331,648 parameters, 8 ranks, bf16), the only one
+that passes through every stage, and the GPT-2-small-sized vector (ZeRO-2,
+8 ranks) with bf16 and with fp16 gradients.  ``--workload`` selects another
+headline; ``--no-also`` leaves the others out.
 
 Prints one JSON line.  ``value`` is whole-job parameters per second with the
 inputs resident in HBM; ``e2e`` is the same metric with the gradients copied
@@ -53,7 +57,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="zero3_24x50m_w8",
+    p.add_argument("--workload", default="gpt2_1p5b_w16_zero1",
                    choices=["zero3_24x50m_w8", "gpt2_small_124m_w8_zero2", "gpt2_1p5b_w16_zero1",
                             "gpt2_small_124m_w8_dp_replicas", "gpt2_small_124m_w8_zero2_offload"])
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None)
@@ -63,6 +67,8 @@ def parse_args(argv=None):
     p.add_argument("--units", type=int, default=None,
                    help="ZeRO-3 only: keep the first N units (a smaller copy of the workload with the same "
                         "per-unit launches, for profiling)")
+    p.add_argument("--no-also", action="store_true",
+                   help="time only the headline workload (not the other configurations under 'also')")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -94,6 +100,15 @@ def layout_sizes(wl):
     units = wl.units() if scheme_of(wl) == 3 else [wl.n]
     padded = [-(-u // W) * W for u in units]
     return sum(padded), padded, units
+
+
+def gather_kernel(wl):
+    """The kernel of a ZeRO-3 step's forward gathers without a hook: all units
+    in one launch (gather_units) when they share one padded shard size whose
+    bytes are a multiple of 32, else two units per launch (copy_segments)."""
+    W = wl.W
+    shards = {-(-u // W) for u in wl.units()}
+    return "gather_units" if len(shards) == 1 and (2 * shards.pop()) % 32 == 0 else "copy_segments"
 
 
 def bytes_per_element(wl):
@@ -149,6 +164,7 @@ def kernel_source_sha256(kernel_sources) -> str:
 
 
 FUSED_SOURCES = ("fused_step.cu", "step_math.cuh")
+COPY_SOURCES = ("copy_cast.cu",)
 REPLICA_SOURCES = ("dp_replicas.cu", "step_math.cuh")
 
 
@@ -345,8 +361,9 @@ def config_of(wl, dtype, gpus):
             "l2": f"inputs larger than L2: {(fused + gathers) / 1e9:.1f} GB touched per step vs "
                   f"{L2_BYTES / 2**20:.0f} MiB of L2",
             "parallelism": "simulated DP ranks in one GPU" + (f"; {gpus} independent replicas" if gpus > 1 else ""),
-            "zero3_schedule": ("per unit: forward gather; backward gather fused into the update pass; one stream "
-                               "(no unit hook registered); the step's launches replayed from a CUDA graph "
+            "zero3_schedule": ("forward gathers of all units in one launch (equal units); per unit, backward gather "
+                               "fused into the update pass; one stream (no unit hook registered); the step's "
+                               "launches replayed from a CUDA graph "
                                "(zero_set_graph), the per-launch timing pass as ordinary launches")
             if scheme_of(wl) == 3 else None}
 
@@ -373,29 +390,22 @@ def whole_job_value(world: int, n: int, steps: int, ms: float) -> float:
 
 # ---- our arm ------------------------------------------------------------------------
 
-def run_ours(args):
+ALSO = (("gpt2_1p5b_w16_zero1", None), ("zero3_24x50m_w8", None), ("gpt2_small_124m_w8_zero2", "bf16"), ("gpt2_small_124m_w8_zero2", "fp16"))
+
+
+def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True):
+    """The step with its inputs resident in HBM: warm-up, then ``args.steps``
+    timed steps (pass 1, CUDA events around the loop on the update stream),
+    then the same steps again with a CUDA event pair around every launch
+    (pass 2, zero_enable_timing) for the per-launch roofline; the brackets
+    cost about 3% of a ZeRO-3 step, so they stay out of pass 1.  Returns
+    (the ZeroStep, its update stream, the step counter reached, the leg's
+    figures)."""
     import torch
     import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    from zero_sharded_mixed_step_gb300 import build
-    build.build()
     import zero_sharded_mixed_step_gb300 as zs
     import workloads as wk
 
-    wl = workload(args.workload, args.units, args.params)
-    dtype = args.dtype or wl.dtypes[0]
-    if wl.dp_replicas:
-        return run_replicas(args, wl, dtype, world, rank, dev)
-    if wl.offload:
-        return run_offload(args, wl, dtype, world, rank, dev)
     scheme = scheme_of(wl)
     n_pad, per_launch, units = layout_sizes(wl)
     su = torch.cuda.Stream(dev)
@@ -405,7 +415,7 @@ def run_ours(args):
         step = zs.ZeroStep(scheme, wl.W, units, dtype, theta0=theta0, device=dev, stream=su, gather_stream=sg,
                            with_grad_buffers=True)
         if scheme == 3:
-            step.set_graph(True)     # the step's 2 U launches replayed from one captured graph
+            step.set_graph(True)     # the step's launches replayed from one captured graph
         del theta0
         for r, d in enumerate(wk.GradSource(wl, dtype, dev).step(1)):
             step.place_(step.grads[r], d)
@@ -417,13 +427,6 @@ def run_ours(args):
         t += 1
         step.step(step.grads, *hp, t)
     torch.cuda.synchronize()
-
-    # ---- timed region: inputs resident in HBM ----------------------------------------
-    # Pass 1 times the steps as they are.  Pass 2 repeats the same steps with a
-    # CUDA event pair recorded around every kernel launch on its own stream
-    # (zero_enable_timing) for the per-launch roofline; the brackets cost
-    # about 3% of a ZeRO-3 step, so they stay out of pass 1.
-    gpu_id = gpu_uuid(dev)
 
     def timed_pass(instrumented: bool):
         nonlocal t
@@ -446,8 +449,13 @@ def run_ours(args):
 
     zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_FUSED)
     zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_GATHER)
-    with ClockSampler(gpu_id) as clocks:
+    if clocks_too:
+        with ClockSampler(gpu_uuid(dev)) as clocks:
+            ms, launches = timed_pass(False)
+        clock_summary = clocks.summary()
+    else:
         ms, launches = timed_pass(False)
+        clock_summary = None
     ms_instr, _ = timed_pass(True)
     fused_ms, fused_n = zs.zero_read_timing(step.ctx, zs.ZERO_KERNEL_FUSED)
     last_variant = step.stat(zs.ZERO_STAT_LAST_VARIANT)
@@ -475,11 +483,50 @@ def run_ours(args):
                 "launches_timed": fused_n, "timing_pass_ms_per_step": ms_instr / args.steps}
     gather_info = None
     if gather_n:
-        # the forward gathers move 2 bytes in and 2 out per element of every unit,
-        # two units per launch (the backward gathers are inside the fused pass)
+        # the forward gathers move 2 bytes in and 2 out per element of every unit
+        # (all units in one launch when they have one size, else two per launch;
+        # the backward gathers are inside the fused pass)
         gather_bytes = 4 * n_pad * args.steps
-        gather_info = {"launch_ms": gather_ms / gather_n, "achieved_gbs": gather_bytes / (gather_ms / 1e3) / 1e9,
-                       "launches": gather_n, "share_of_bracketed_time": gather_ms / (gather_ms + fused_ms)}
+        achieved_g = gather_bytes / (gather_ms / 1e3) / 1e9
+        kernel = gather_kernel(wl)
+        gather_info = {"kernel": kernel, "launch_ms": gather_ms / gather_n, "achieved_gbs": achieved_g,
+                       "frac": achieved_g / peak, "launches": gather_n,
+                       "bytes_per_launch": gather_bytes // gather_n,
+                       "traffic": recorded_traffic(f"{kernel}_{wl.name}", COPY_SOURCES),
+                       "share_of_bracketed_time": gather_ms / (gather_ms + fused_ms)}
+    leg = {"workload": wl.name, "grad_dtype": dtype, "value": value, "unit": "params/s", "ms_per_step": ms_per_step,
+           "steps": args.steps, "warmup": args.warmup, "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
+           "algorithmic_bytes_per_step": fused_b + gather_b, "roofline": roofline, "gather": gather_info,
+           "gpu_launches": launches, "clocks": clock_summary}
+    return step, su, t, leg
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from zero_sharded_mixed_step_gb300 import build
+    build.build()
+    import zero_sharded_mixed_step_gb300 as zs
+
+    wl = workload(args.workload, args.units, args.params)
+    dtype = args.dtype or wl.dtypes[0]
+    if wl.dp_replicas:
+        return run_replicas(args, wl, dtype, world, rank, dev)
+    if wl.offload:
+        return run_offload(args, wl, dtype, world, rank, dev)
+    scheme = scheme_of(wl)
+    n_pad, per_launch, units = layout_sizes(wl)
+    step, su, t, leg = device_leg(args, wl, dtype, dev, world)
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
 
     # ---- end to end: gradients from page-locked host memory, working copy read back --
     # through zero_step_host, the C-ABI call that takes host buffers: each step
@@ -547,19 +594,39 @@ def run_ours(args):
             b.close()
 
     step.close()
+    del step
+    torch.cuda.empty_cache()
+
+    # the other configurations, on the device only, one at a time (each
+    # freed before the next), after the headline's timed regions
+    also = {}
+    if not args.no_also and args.units is None and args.params is None:
+        for name, dt in ALSO:
+            other = workload(name)
+            dt = dt or other.dtypes[0]
+            if other.name == wl.name and dt == dtype:
+                continue
+            o_step, _, _, o_leg = device_leg(args, other, dt, dev, world, clocks_too=True)
+            o_step.close()
+            del o_step
+            torch.cuda.empty_cache()
+            o_leg["config"] = config_of(other, dt, world)
+            also[f"{name}_{dt}" if name.startswith("gpt2_small") else name] = o_leg
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, dtype, args.cpu_seconds)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "metric": METRIC, "value": leg["value"], "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": leg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_of(wl, dtype, world),
-            "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
-            "roofline": roofline, "gather": gather_info, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks.summary(),
+            "step_hbm_gbs": leg["step_hbm_gbs"], "step_frac_of_peak": leg["step_frac_of_peak"],
+            "roofline": leg["roofline"], "gather": leg["gather"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": leg["gpu_launches"], "clocks": leg["clocks"],
+            "also": also or None,
         }
         print(json.dumps(line))
     if world > 1:
