@@ -294,20 +294,26 @@ def cpu_cores_note():
     return n, model
 
 
+SAMPLE_CAP = 1 << 24
+
+
 def calibrate_sample(wl, dtype, budget_s):
-    """Sample size whose oracle step takes about budget_s seconds."""
+    """Sample size whose oracle step takes about budget_s seconds, at most
+    2^24 parameters (the oracle's elementwise rate does not depend on the
+    size beyond that, and its host memory does: about 220 bytes per
+    parameter at W = 16)."""
     dt, n = oracle_sample_step_seconds(wl, 1 << 20, dtype)
     per = dt / n
-    return int(max(1 << 18, min(budget_s / per, wl.n)))
+    return int(max(1 << 18, min(budget_s / per, wl.n, SAMPLE_CAP)))
 
 
 def cpu_baseline(wl, dtype, budget_s):
     """The oracle as it stands, timed on this host for about ``budget_s``
     seconds: a sample sized so that one step takes about that long (capped
-    at the workload, or at one unit for ZeRO-3), run for as many steps as
-    the budget holds (at most 20)."""
+    at the workload, at one unit for ZeRO-3, and at 2^24 parameters), run
+    for as many steps as the budget holds (at most 100)."""
     size = calibrate_sample(wl, dtype, budget_s)
-    dt, n, steps = oracle_sample_steps(wl, size, dtype, budget_s, max_steps=20)
+    dt, n, steps = oracle_sample_steps(wl, size, dtype, budget_s, max_steps=100)
     host_cores, model = cpu_cores_note()
     what = (f"{steps} step(s) (t = 1..{steps}) of the oracle on {n:,} of the {wl.n:,} parameters "
             + ("(one unit shrunk to that size, full ZeRO-3 schedule)" if scheme_of(wl) == 3 else "(leading slice)")
