@@ -540,12 +540,15 @@ def run_ours(args):
     # staging ring and returns the updated 16-bit working copy to host memory,
     # pipelined chunk by chunk (unit by unit for ZeRO-3) on three streams.
     e2e = None
-    if not args.no_e2e and args.e2e_steps > 0:
+    out_elems = step.n_pad if scheme != 3 else wl.W * step.sizes["shard_store"]
+    e2e_room = host_room_for(2 * (wl.W * step.n_pad + out_elems), world)
+    if not args.no_e2e and args.e2e_steps > 0 and e2e_room is not None:
+        e2e = {"skipped": e2e_room}
+    elif not args.no_e2e and args.e2e_steps > 0:
         # host buffers from zero_host_alloc: page-locked on huge pages, where the
         # link holds its full rate (memory from cudaHostAlloc measured slower)
         # one block for the W gradient vectors and the read-back (all 16-bit),
         # so that even vectors smaller than a huge page sit on huge pages
-        out_elems = step.n_pad if scheme != 3 else wl.W * step.sizes["shard_store"]
         need = zs.zero_host_staging_bytes(scheme, wl.W, units, 0)
         staging = torch.empty(need, dtype=torch.uint8, device=dev)
         sh, sd = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -736,10 +739,11 @@ def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
     tried = []
     for _ in range(attempts):
         if tried:
-            # another block only while the host keeps room for two more
-            # (several ranks on one host each hold their own blocks)
+            # another block only while the host keeps room for two more for
+            # every process on it (several ranks on one host each hold their own)
             avail = host_mem_available()
-            if avail is not None and avail < 2 * 2 * elems16:
+            local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+            if avail is not None and avail < 2 * 2 * elems16 * local:
                 break
             try:
                 hb = zs.HostBuffer(elems16, torch.int16)
@@ -759,6 +763,21 @@ def settled_host_block(elems16: int, views_of, probe_of, attempts: int = 3):
     best[2]["host_block_attempts"] = len(tried)
     spares = [hb for hb, _, _ in tried if hb is not best[0]]
     return best[0], best[1], best[2], spares
+
+
+def host_room_for(block_bytes: int, world: int) -> str | None:
+    """None when every process on this host can take a page-locked block of
+    ``block_bytes`` for the end-to-end leg (with a quarter of the available
+    memory to spare), else the reason it cannot.  Decided the same way on
+    every rank (a max over ranks), so that all of them run the leg's
+    collectives or none does."""
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_mem_available()
+    short = avail is not None and block_bytes * local > 0.75 * avail
+    if max_over_ranks(1.0 if short else 0.0) == 0.0:
+        return None
+    return (f"host memory: the end-to-end leg page-locks {block_bytes / 1e9:.1f} GB per process, "
+            f"{local} process(es) on this host, {((avail or 0) / 1e9):.1f} GB available on the one that ran short")
 
 
 def host_mem_available() -> int | None:
@@ -813,6 +832,9 @@ def e2e_through_torch_copies(args, world, wl, su, grads, result, run_step, t0, p
     # one block for the W gradient vectors and the read-back (all 16-bit), so
     # that even vectors smaller than a huge page sit on huge pages
     n, W = grads[0].numel(), len(grads)
+    room = host_room_for(2 * (W * n + result.numel()), world)
+    if room is not None:
+        return {"skipped": room}, t0
 
     def views_of(block):
         grads_h = [block[r * n:(r + 1) * n].view(grads[0].dtype) for r in range(W)]

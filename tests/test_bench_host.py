@@ -188,3 +188,34 @@ def test_settled_host_block_stops_retrying_when_memory_runs_short(monkeypatch):
     monkeypatch.setattr(FakeBlock, "__init__", init_then_fail)
     block, _, probe, spares = bench.settled_host_block(64, lambda t: None, probe_of)
     assert probe["host_block_attempts"] == 1 and spares == [] and len(made) == 1
+
+
+def _room_rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), LOCAL_WORLD_SIZE=str(world))
+    # rank 1's host reports less memory than two 40 GB blocks need; rank 0's is ample
+    bench.host_mem_available = (lambda: 90 * 10**9) if rank == 1 else (lambda: 10**12)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    out[rank] = (bench.host_room_for(40 * 10**9, world), bench.host_room_for(10 * 10**9, world))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_end_to_end_leg_is_skipped_on_every_rank_when_one_host_is_short():
+    """The end-to-end leg page-locks a block per process; when one rank's
+    host cannot hold a block for every local process, all ranks skip the
+    leg (so the collectives inside it stay matched) and say why."""
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = 29500 + (os.getpid() + 977) % 2000
+        procs = [ctx.Process(target=_room_rank, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        for r in range(2):
+            big, small = out[r]
+            assert big is not None and "host memory" in big and "2 process(es)" in big
+            assert small is None
