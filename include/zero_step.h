@@ -435,11 +435,15 @@ int zero_set_variant(zero_ctx* ctx, int variant);
 /*
  * ZeRO-3 steps from a CUDA graph (on != 0) or as ordinary launches (0, the
  * default).  With it on, the first zero_step that runs without a unit hook,
- * timing brackets, debug flags or an injected stall captures its U + U/2
- * launches (rounded up) into a graph; that step and every later one with the same
- * conditions set the fused kernels' Adam coefficients and gradient pointers
- * on the graph and launch it once on the update stream, which saves the gaps
- * between the launches.  Steps under other conditions run the ordinary
+ * timing brackets, debug flags or an injected stall captures its launches
+ * (the forward gathers, then U update passes) into a graph; that step and
+ * every later one with the same conditions set the fused kernels' Adam
+ * coefficients and gradient pointers on the graph and launch it once on the
+ * update stream, which saves the gaps between the launches.  In the graph
+ * the backward update passes form two chains (alternate units, each chain
+ * holding the units that share a unit buffer), so that one unit's pass can
+ * take SMs as the other's frees them; the graph orders everything the
+ * schedule's data needs.  Steps under other conditions run the ordinary
  * launches; results are bit-identical either way and the counters advance
  * the same.  ZERO_E_ARG for a scheme other than ZeRO-3 (one launch per step:
  * nothing to capture) or a context whose update stream is the legacy default

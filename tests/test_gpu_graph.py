@@ -75,15 +75,18 @@ def _graph_steps_equal_launched_steps():
     graph.close()
 
 
-def test_graph_steps_fall_back_and_recapture():
+@pytest.mark.parametrize("units", [[262_144, 262_147, 100_000], [262_144, 262_144, 262_144]],
+                         ids=["ragged", "one_size"])
+def test_graph_steps_fall_back_and_recapture(units):
     """A hook, timing brackets and a variant change run the ordinary launches
-    (or capture anew); every step still matches the plain context."""
+    (or capture anew); every step still matches the plain context.  Units of
+    one size take the one-launch forward gathers, ragged ones a launch per
+    pair, in the graph and outside it."""
     with torch.cuda.stream(_stream()):
-        _graph_steps_fall_back_and_recapture()
+        _graph_steps_fall_back_and_recapture(units)
 
 
-def _graph_steps_fall_back_and_recapture():
-    units = [262_144, 262_147, 100_000]
+def _graph_steps_fall_back_and_recapture(units):
     wl, (plain, graph) = _pair(units, 8, "fp16")
     src = wk.GradSource(wl, "fp16", "cuda")
     hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
@@ -108,6 +111,8 @@ def _graph_steps_fall_back_and_recapture():
     assert len(calls) == 2 * len(units)          # the hooked step ran unit by unit
     ms, n = zs.zero_read_timing(graph.ctx, zs.ZERO_KERNEL_FUSED)
     assert n == len(units)                        # the timed step ran as ordinary launches
+    ms, n = zs.zero_read_timing(graph.ctx, zs.ZERO_KERNEL_GATHER)
+    assert n == (1 if len(set(units)) == 1 else (len(units) + 1) // 2)   # its forward gathers
     graph.set_graph(False)
     plain.close()
     graph.close()

@@ -82,6 +82,8 @@ int ensure_cuda(zero_ctx* c) {
     ZERO_CUDA(cudaEventCreateWithFlags(&c->ev_updated[b], cudaEventDisableTiming));
   }
   ZERO_CUDA(cudaEventCreateWithFlags(&c->ev_out_done, cudaEventDisableTiming));
+  ZERO_CUDA(cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming));
+  ZERO_CUDA(cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming));
   c->cuda_ready = true;
   return ZERO_OK;
 }
@@ -326,6 +328,9 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
   bool used[2] = {false, false};
   int64_t held[2] = {0, 0};
   int64_t seq = 0;
+  // the stream of the fused backward pass (without a hook): su, or the
+  // second chain of a captured step (see below)
+  cudaStream_t s_upd = su;
   auto unit = [&](int64_t u, int phase) -> int {
     Range range(phase == 0 ? "zero3 forward unit %lld" : "zero3 backward unit %lld", static_cast<long long>(u));
     const int b = static_cast<int>(seq++ & 1);
@@ -339,10 +344,10 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
     if (phase == 1 && c->hook == nullptr) {
       // nothing runs between this unit's gather and its update, so one pass
       // does both: it copies the pre-update 16-bit values out, then updates
-      r = launch_update(c, u, grads, coef, su, buf);
+      r = launch_update(c, u, grads, coef, s_upd, buf);
       if (r) return r;
       count_scatter(c, u);
-      if ((r = poison_unit(c, u, buf, su))) return r;
+      if ((r = poison_unit(c, u, buf, s_upd))) return r;
       used[b] = true;
       return ZERO_OK;
     }
@@ -415,9 +420,27 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
       if (rc) return rc;
     }
   }
-  for (int64_t u = U - 1; u >= 0; --u) {
+  // Backward.  While a step is being captured (no hook, no poisoning), the
+  // fused passes go on two chains: backward units k = 0, 2, 4, ... on su and
+  // k = 1, 3, ... on a second stream, both after the forward gathers.  A
+  // unit's pass writes only its own range of the state, its shard slots and
+  // its unit buffer, and the units that share a buffer (k and k + 2) are on
+  // one chain, in order; so the graph orders exactly what must be ordered,
+  // and a unit's CTAs can take the SMs that the one before it frees instead
+  // of waiting for all of them.
+  const bool chains = c->capturing && c->s_alt != nullptr && c->hook == nullptr && c->debug == 0;
+  if (chains) {
+    ZERO_CUDA(cudaEventRecord(c->ev_fork, su));
+    ZERO_CUDA(cudaStreamWaitEvent(c->s_alt, c->ev_fork, 0));
+  }
+  for (int64_t u = U - 1, k = 0; u >= 0; --u, ++k) {
+    s_upd = chains && (k & 1) ? c->s_alt : su;
     rc = unit(u, 1);
     if (rc) return rc;
+  }
+  if (chains) {
+    ZERO_CUDA(cudaEventRecord(c->ev_join, c->s_alt));
+    ZERO_CUDA(cudaStreamWaitEvent(su, c->ev_join, 0));
   }
   c->live_elems -= held[0] + held[1];
   return ZERO_OK;
@@ -457,10 +480,14 @@ int capture_zero3(zero_ctx* c, const void* const* grads, const zero::AdamCoef& c
     if (e0 != cudaSuccess) return cuda_fail(e0, "clearing the device error counter");
     c->err_slot_ready = true;
   }
+  // the stream of the second backward chain (created once, outside the capture)
+  if (c->s_alt == nullptr) ZERO_CUDA(cudaStreamCreateWithFlags(&c->s_alt, cudaStreamNonBlocking));
   const int64_t comm = c->comm, launches = c->launches, gathers = c->gathers, scatters = c->scatters;
   const int64_t live = c->live_elems, peak = c->peak_live;
   ZERO_CUDA(cudaStreamBeginCapture(c->su, cudaStreamCaptureModeThreadLocal));
+  c->capturing = true;
   rc = run_zero3_step(c, grads, coef);
+  c->capturing = false;
   cudaGraph_t g = nullptr;
   const cudaError_t e = cudaStreamEndCapture(c->su, &g);
   c->graph_comm = c->comm - comm;
@@ -690,7 +717,10 @@ int zero_destroy(zero_ctx* c) {
       cudaEventDestroy(c->ev_updated[b]);
     }
     cudaEventDestroy(c->ev_out_done);
+    cudaEventDestroy(c->ev_fork);
+    cudaEventDestroy(c->ev_join);
   }
+  if (c->s_alt) cudaStreamDestroy(c->s_alt);
   delete c;
   return rc;
 }

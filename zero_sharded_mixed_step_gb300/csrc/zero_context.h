@@ -84,6 +84,9 @@ struct zero_ctx {
   cudaEvent_t ev_begin = nullptr, ev_gathered[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
   cudaEvent_t ev_landed[2] = {nullptr, nullptr}, ev_slot_free[2] = {nullptr, nullptr};
   cudaEvent_t ev_updated[2] = {nullptr, nullptr}, ev_out_done = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;   // the two backward chains of a captured step
+  cudaStream_t s_alt = nullptr;                       // the second chain's stream (owned)
+  bool capturing = false;                             // a ZeRO-3 step is being captured
   std::vector<cudaStream_t> touched;
   int variant = ZERO_VARIANT_AUTO;
   int64_t t = 0;
