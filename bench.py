@@ -368,9 +368,9 @@ def config_of(wl, dtype, gpus):
                   f"{L2_BYTES / 2**20:.0f} MiB of L2",
             "parallelism": "simulated DP ranks in one GPU" + (f"; {gpus} independent replicas" if gpus > 1 else ""),
             "zero3_schedule": ("forward gathers of all units in one launch (equal units); per unit, backward gather "
-                               "fused into the update pass; one stream (no unit hook registered); the step's "
-                               "launches replayed from a CUDA graph "
-                               "(zero_set_graph), the per-launch timing pass as ordinary launches")
+                               "fused into the update pass (no unit hook registered); the step's launches "
+                               "replayed from a CUDA graph (zero_set_graph), its backward passes on two chains of "
+                               "alternate units; the per-launch timing pass as ordinary launches on one stream")
             if scheme_of(wl) == 3 else None}
 
 
