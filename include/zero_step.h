@@ -270,7 +270,9 @@ int zero_step_bucket(zero_ctx* ctx, int64_t lo, int64_t len, const void* const* 
 /*
  * Device bytes of the staging ring zero_step_host needs: two slots, each
  * holding every rank's gradients for one chunk (DP/Z1/Z2: chunk_elems
- * values, 0 meaning 16,777,216; ZeRO-3: one unit, max_u S_u * W values), in
+ * values, 0 meaning the default: n_pad / 24 rounded up to a multiple of
+ * 2^20 and kept between 2^24 and 2^26; ZeRO-3: one unit, max_u S_u * W
+ * values), in
  * the gradient format: 2 * W * round_up((chunk + 8) * 2, 256).  The ring
  * stays this size whatever n is: the constant-size buffers of "One Poem
  * Suffices: ZeRO" section 4.2.2 (C_B) instead of W full gradient vectors on

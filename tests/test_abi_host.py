@@ -229,6 +229,12 @@ def test_host_staging_bytes(zlib):
     assert zs.zero_host_staging_bytes(1, 8, [10_000_000], 1 << 20) == 2 * 8 * (((1 << 20) + 8) * 2 + 255) // 256 * 256
     assert zs.zero_host_staging_bytes(1, 4, [100], 0) == 2 * 4 * (((1 << 24) + 8) * 2 + 255) // 256 * 256
     assert zs.zero_host_staging_bytes(2, 8, [100], 13) == 2 * 8 * 256       # chunk rounds up to 16 elements
+    # the default chunk: about 24 per step, in multiples of 2^20, between 2^24 and 2^26
+    def slots(W, chunk):
+        return 2 * W * (((chunk + 8) * 2 + 255) // 256 * 256)
+    assert zs.zero_host_staging_bytes(2, 8, [124_439_808], 0) == slots(8, 1 << 24)
+    assert zs.zero_host_staging_bytes(1, 16, [1_557_611_200], 0) == slots(16, 62 << 20)   # 64,900,467 rounded up
+    assert zs.zero_host_staging_bytes(1, 1, [10**10], 0) == slots(1, 1 << 26)
     units = [50_331_648] * 24
     assert zs.zero_host_staging_bytes(3, 8, units, 0) == 2 * 8 * ((50_331_648 + 8) * 2 + 255) // 256 * 256
     assert _err(zs.zero_host_staging_bytes, 1, 8, [10, 10], 0) == zs.ZERO_E_ARG
