@@ -169,8 +169,8 @@ def test_zero3_backward_gather_fused_into_update():
         assert not torch.equal(before, s.working_copy())
     L = z.Layout(wl.W, units)
     assert zs.zero_comm_bytes_per_rank(s.ctx) == 2 * 3 * sum(z.ring_bytes_per_rank(wl.W, x) for x in L.S)
-    # a cast per unit, then per step the forward gathers two units per launch and
-    # one pass per unit gathers and updates it
+    # a cast per unit, then per step the forward gathers two units per launch (the
+    # units have different sizes) and one pass per unit gathers and updates it
     U = len(units)
     assert s.stat(zs.ZERO_STAT_LAUNCHES) == U + 2 * ((U + 1) // 2 + U)
     s.close()
