@@ -310,10 +310,9 @@ int poison_unit(zero_ctx* c, int64_t u, void* buf, cudaStream_t s) {
 // forward gathers go in one launch when every unit has the same shard size
 // (zero::launch_gather_units: pair after pair of units, each buffer position
 // receiving its units in unit order), else two units per launch (one into
-// each buffer), and each
-// backward gather is done by its unit's update pass.  A unit counts as live
-// from its gather until its buffer is taken by a later gather (or the step
-// ends): at most two units are live.
+// each buffer), and each backward gather is done by its unit's update pass.
+// A unit counts as live from its gather until its buffer is taken by a later
+// gather (or the step ends): at most two units are live.
 int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& coef) {
   int rc = ensure_cuda(c);
   if (rc) return rc;
@@ -435,24 +434,25 @@ int run_zero3_step(zero_ctx* c, const void* const* grads, const zero::AdamCoef& 
   }
   for (int64_t u = U - 1, k = 0; u >= 0; --u, ++k) {
     s_upd = chains && (k & 1) ? c->s_alt : su;
-    rc = unit(u, 1);
-    if (rc) return rc;
+    if ((rc = unit(u, 1))) break;
   }
-  if (chains) {
+  if (chains) {   // joined even after a failed launch, so that the capture ends cleanly
     ZERO_CUDA(cudaEventRecord(c->ev_join, c->s_alt));
     ZERO_CUDA(cudaStreamWaitEvent(su, c->ev_join, 0));
   }
+  if (rc) return rc;
   c->live_elems -= held[0] + held[1];
   return ZERO_OK;
 }
 
 // ---- ZeRO-3 steps replayed from a CUDA graph ----------------------------------------
 //
-// A ZeRO-3 step without a hook is a fixed sequence of launches on one stream
-// (the forward gathers, then one update per unit).  Captured once, it is replayed as one graph launch, which saves the
-// launch gaps between its kernels; only the fused kernels' Adam coefficients
-// and gradient pointers change from step to step, and they are set on the
-// graph's nodes before each replay.
+// A ZeRO-3 step without a hook is a fixed set of launches: the forward
+// gathers, then one update per unit (on two chains in the graph, see
+// run_zero3_step).  Captured once, it is replayed as one graph launch, which
+// saves the launch gaps between its kernels; only the fused kernels' Adam
+// coefficients and gradient pointers change from step to step, and they are
+// set on the graph's nodes before each replay.
 
 void drop_graph(zero_ctx* c) {
   if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
