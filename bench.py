@@ -777,7 +777,8 @@ def host_room_for(block_bytes: int, world: int) -> str | None:
     if max_over_ranks(1.0 if short else 0.0) == 0.0:
         return None
     return (f"host memory: the end-to-end leg page-locks {block_bytes / 1e9:.1f} GB per process, "
-            f"{local} process(es) on this host, {((avail or 0) / 1e9):.1f} GB available on the one that ran short")
+            f"{local} process(es) per host; this host has {((avail or 0) / 1e9):.1f} GB available"
+            + ("" if short else ", another rank's host ran short"))
 
 
 def host_mem_available() -> int | None:
