@@ -444,10 +444,10 @@ def load_peak_pins():
 
 
 def check_peak_bytes(z):
-    """Peak bytes of a ZeRO-3 rank against what the pages state: "own shard
-    plus one borrowed layer" ("ZeRO, annotated", section 7, stage 3 step by
-    step) and 2/64 of the parameters at peak on 64 devices ("One Poem
-    Suffices: ZeRO", section 4.1.4).  The 64-device case runs the oracle's
+    """Peak bytes of a ZeRO-3 rank against what the pages state: a GPU holds
+    at most its own shard and the one layer lent to it ("ZeRO, annotated",
+    section 7, stage 3 step by step), and parameters worth 2/64 of the model
+    at peak on 64 devices ("One Poem Suffices: ZeRO", section 4.1.4).  The 64-device case runs the oracle's
     ZeRO-3 schedule on the scaled model and takes the gathered values from
     what the schedule held live, not from the row."""
     rows = load_peak_pins()
@@ -473,7 +473,7 @@ def check_peak_bytes(z):
         assert param_bytes == z.B_P16 * row["elems"], (row["id"], param_bytes)
         if row["printed"].startswith("2/64"):
             assert 64 * row["elems"] == 2 * psi, row["id"]
-        else:                                  # own shard plus one borrowed layer of one shard
+        else:                                  # the rank's shard and one lent layer of one shard
             assert row["elems"] == 2 * S and gathered == S, row["id"]
         # the other schemes gather nothing: their peak is what they hold
         for scheme in (z.DP, z.ZERO1, z.ZERO2):
