@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kCopyThreads) cast_segments(const __grid_const
 // two-unit launch below the copy rate.
 constexpr int kGatherThreads = 256;
 constexpr int kGatherVec = 32;     // bytes per access
-constexpr int kGatherUnroll = 2;   // accesses in flight per thread
+constexpr int kGatherUnroll = 3;   // accesses in flight per thread
 
 struct UnitGatherArgs {
   const void* shard[kMaxRanks];   // rank r's store; unit u's shard at u * S values
@@ -225,10 +225,19 @@ cudaError_t launch_gather_units(const void* const* shard, int W, void* const* bu
   g.tiles_per_rank = (g.nvec + kGatherThreads * kGatherUnroll - 1) / (kGatherThreads * kGatherUnroll);
   g.W = W;
   g.nbuf = units >= 2 ? 2 : 1;
+  // Blocks of 256 threads, between 1.5 and 2 per SM, as many as split each
+  // pair's tiles evenly (every block the same number, so that none finishes
+  // a tile behind the others pair after pair); two per SM when no count in
+  // that range does.  Measured on GB300 over the 24 x 50,331,648-value
+  // units (W = 8): 3 accesses of 32 bytes per thread on 256 blocks (32 tiles
+  // each per pair) took 704 us; 3 accesses on 304 blocks 735 us, and 2 or 4
+  // accesses on 256 to 768 blocks 728-814 us.
   const int64_t total = g.tiles_per_rank * W * g.nbuf;
-  // two resident blocks of 256 threads per SM: copies measured fastest at 512
-  // threads per SM with 64 bytes in flight per thread
-  int64_t blocks = static_cast<int64_t>(sm_count()) * 2;
+  const int64_t sms = sm_count();
+  int64_t blocks = 0;
+  for (int64_t b = 2 * sms; b >= (3 * sms + 1) / 2 && blocks == 0; --b)
+    if (total % b == 0) blocks = b;
+  if (blocks == 0) blocks = 2 * sms;
   if (blocks > total) blocks = total;
   gather_units<<<static_cast<unsigned>(blocks), kGatherThreads, 0, stream>>>(g);
   ++*launches;
