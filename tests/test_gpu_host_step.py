@@ -167,3 +167,50 @@ def test_host_step_with_the_benchmark_units():
     block.close()
     a.close()
     b.close()
+
+
+def test_host_step_with_the_headline_chunking():
+    """The GPT-2-1.5B workload's ranks and format (W = 16, fp16, ZeRO-1) on a
+    vector long enough that the default chunk is above 2^24 elements
+    (25 x 2^24 + 12,345 parameters: chunks of 17,825,792), fed from one
+    huge-page block the way the benchmark's end-to-end leg feeds it: two
+    steps, bit-identical to the device step, the read-back equal to the
+    device's working copy."""
+    n = 25 * (1 << 24) + 12_345
+    wl = wk.scaled(wk.GPT2_XL, n=n, steps=2, name="headline_chunking")
+    W = wl.W
+    theta0 = wk.draw_theta0(wl, "cuda")
+    a = zs.ZeroStep(zs.ZERO_SCHEME_Z1, W, [n], "fp16", theta0=theta0, with_grad_buffers=True)
+    b = zs.ZeroStep(zs.ZERO_SCHEME_Z1, W, [n], "fp16", theta0=theta0)
+    del theta0
+    n_pad = a.n_pad
+    chunk = -(-(-(-n_pad // 24)) // (1 << 20)) * (1 << 20)        # n_pad / 24, up to a multiple of 2^20
+    assert chunk > 1 << 24
+    need = zs.zero_host_staging_bytes(zs.ZERO_SCHEME_Z1, W, [n], 0)
+    assert need == 2 * W * (((chunk + 8) * 2 + 255) // 256 * 256)
+    staging = torch.empty(need, dtype=torch.uint8, device="cuda")
+    block = zs.HostBuffer(W * n_pad + n_pad, torch.int16)
+    host = [block.tensor[r * n_pad:(r + 1) * n_pad].view(torch.float16) for r in range(W)]
+    host_out = block.tensor[W * n_pad:].view(torch.float16)
+    sh, sd = torch.cuda.Stream(), torch.cuda.Stream()
+    src = wk.GradSource(wl, "fp16", "cuda")
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    for t in range(1, wl.steps + 1):
+        for g, d in zip(a.grads, src.step(t)):
+            a.place_(g, d)
+            del d
+        for h, g in zip(host, a.grads):
+            h.copy_(g)
+        torch.cuda.synchronize()
+        a.step(a.grads, *hp, t)
+        zs.zero_step_host(b.ctx, zs.ZERO_SCHEME_Z1, W, n, host, host_out, staging, need, 0, *hp, t, sh, sd)
+        b.sync(timeout_ms=120_000)
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
+        assert torch.equal(a.p16.view(torch.int16), b.p16.view(torch.int16)), t
+        assert torch.equal(host_out.view(torch.int16), b.p16.cpu().view(torch.int16)), t
+    assert a.stat(zs.ZERO_STAT_COMM_BYTES) == b.stat(zs.ZERO_STAT_COMM_BYTES)
+    del host, host_out
+    block.close()
+    a.close()
+    b.close()
