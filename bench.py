@@ -396,16 +396,22 @@ def whole_job_value(world: int, n: int, steps: int, ms: float) -> float:
 
 # ---- our arm ------------------------------------------------------------------------
 
-ALSO = (("gpt2_1p5b_w16_zero1", None), ("zero3_24x50m_w8", None), ("gpt2_small_124m_w8_zero2", "bf16"), ("gpt2_small_124m_w8_zero2", "fp16"))
+# (workload, gradient format, bucket elements: the step applied bucket by bucket with zero_step_bucket)
+ALSO = (("gpt2_1p5b_w16_zero1", None, None), ("zero3_24x50m_w8", None, None),
+        ("gpt2_small_124m_w8_zero2", "bf16", None), ("gpt2_small_124m_w8_zero2", "fp16", None),
+        ("gpt2_small_124m_w8_zero2", "bf16", 1 << 24))
 
 
-def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True):
+def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elems=None):
     """The step with its inputs resident in HBM: warm-up, then ``args.steps``
     timed steps (pass 1, CUDA events around the loop on the update stream),
     then the same steps again with a CUDA event pair around every launch
     (pass 2, zero_enable_timing) for the per-launch roofline; the brackets
-    cost about 3% of a ZeRO-3 step, so they stay out of pass 1.  Returns
-    (the ZeroStep, its update stream, the step counter reached, the leg's
+    cost about 3% of a ZeRO-3 step, so they stay out of pass 1.  With
+    ``bucket_elems`` (DP/Z1/Z2) each step is applied bucket by bucket
+    (zero_step_bucket), each bucket reading its range of the gradient
+    vectors, as the buckets of a backward pass would arrive.  Returns (the
+    ZeroStep, its update stream, the step counter reached, the leg's
     figures)."""
     import torch
     import torch.distributed as dist
@@ -428,10 +434,23 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True):
             del d
     torch.cuda.synchronize()
     hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    buckets = None
+    if bucket_elems:
+        # each bucket's gradient pointers into the W vectors, built once
+        buckets = [(lo, min(bucket_elems, n_pad - lo), [g.data_ptr() + 2 * lo for g in step.grads])
+                   for lo in range(0, n_pad, bucket_elems)]
+
+    def one_step(t):
+        if buckets is None:
+            step.step(step.grads, *hp, t)
+        else:
+            for lo, length, ptrs in buckets:
+                zs.zero_step_bucket(step.ctx, lo, length, ptrs, *hp, t, su)
+
     t = 0
     for _ in range(args.warmup):
         t += 1
-        step.step(step.grads, *hp, t)
+        one_step(t)
     torch.cuda.synchronize()
 
     def timed_pass(instrumented: bool):
@@ -445,7 +464,7 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True):
         e0.record(su)
         for _ in range(args.steps):
             t += 1
-            step.step(step.grads, *hp, t)
+            one_step(t)
         e1.record(su)
         torch.cuda.synchronize()
         zs.zero_enable_timing(step.ctx, False)
@@ -477,7 +496,7 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True):
     # gather (2 bytes read + 2 written per element on top of 2 W + 26).
     peak, peak_src = hbm_peak()
     per_elem = 2 * wl.W + 26 + (4 if scheme == 3 else 0)
-    per_launch_bytes = per_elem * per_launch[0]
+    per_launch_bytes = per_elem * (per_launch[0] if buckets is None else n_pad // len(buckets))
     fused_avg_ms = fused_ms / max(1, fused_n)
     achieved = per_launch_bytes / (fused_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -501,6 +520,8 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True):
                        "traffic": recorded_traffic(f"{kernel}_{wl.name}", COPY_SOURCES),
                        "share_of_bracketed_time": gather_ms / (gather_ms + fused_ms)}
     leg = {"workload": wl.name, "grad_dtype": dtype, "value": value, "unit": "params/s", "ms_per_step": ms_per_step,
+           "buckets": None if buckets is None else {"bucket_elems": bucket_elems, "per_step": len(buckets),
+                                                    "entry_point": "zero_step_bucket"},
            "steps": args.steps, "warmup": args.warmup, "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
            "algorithmic_bytes_per_step": fused_b + gather_b, "roofline": roofline, "gather": gather_info,
            "gpu_launches": launches, "clocks": clock_summary}
@@ -610,17 +631,20 @@ def run_ours(args):
     # freed before the next), after the headline's timed regions
     also = {}
     if not args.no_also and args.units is None and args.params is None:
-        for name, dt in ALSO:
+        for name, dt, bucket in ALSO:
             other = workload(name)
             dt = dt or other.dtypes[0]
-            if other.name == wl.name and dt == dtype:
+            if other.name == wl.name and dt == dtype and bucket is None:
                 continue
-            o_step, _, _, o_leg = device_leg(args, other, dt, dev, world, clocks_too=True)
+            o_step, _, _, o_leg = device_leg(args, other, dt, dev, world, clocks_too=True, bucket_elems=bucket)
             o_step.close()
             del o_step
             torch.cuda.empty_cache()
             o_leg["config"] = config_of(other, dt, world)
-            also[f"{name}_{dt}" if name.startswith("gpt2_small") else name] = o_leg
+            key = f"{name}_{dt}" if name.startswith("gpt2_small") else name
+            if bucket:
+                key += f"_buckets_of_2p{bucket.bit_length() - 1}"
+            also[key] = o_leg
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
