@@ -12,7 +12,8 @@ ranks, fp16, ZeRO-1).  The same process then times the other configurations
 on the device and reports them under ``also``: the ZeRO-3 layer-unit
 schedule (24 units of 50,331,648 parameters, 8 ranks, bf16), the only one
 that passes through every stage, and the GPT-2-small-sized vector (ZeRO-2,
-8 ranks) with bf16 and with fp16 gradients.  ``--workload`` selects another
+8 ranks) with bf16 and with fp16 gradients, and with bf16 applied bucket by
+bucket (zero_step_bucket, 8 buckets of 2^24).  ``--workload`` selects another
 headline; ``--no-also`` leaves the others out.
 
 Prints one JSON line.  ``value`` is whole-job parameters per second with the
