@@ -12,8 +12,9 @@ ranks, fp16, ZeRO-1).  The same process then times the other configurations
 on the device and reports them under ``also``: the ZeRO-3 layer-unit
 schedule (24 units of 50,331,648 parameters, 8 ranks, bf16), the only one
 that passes through every stage, and the GPT-2-small-sized vector (ZeRO-2,
-8 ranks) with bf16 and with fp16 gradients, and with bf16 applied bucket by
-bucket (zero_step_bucket, 8 buckets of 2^24).  ``--workload`` selects another
+8 ranks) with bf16 and with fp16 gradients, with bf16 applied bucket by
+bucket (zero_step_bucket, 8 buckets of 2^24), as data parallelism with its 8
+replicas kept literally, and as ZeRO-2 with the optimizer on the host.  ``--workload`` selects another
 headline; ``--no-also`` leaves the others out.
 
 Prints one JSON line.  ``value`` is whole-job parameters per second with the
@@ -400,7 +401,8 @@ def whole_job_value(world: int, n: int, steps: int, ms: float) -> float:
 # (workload, gradient format, bucket elements: the step applied bucket by bucket with zero_step_bucket)
 ALSO = (("gpt2_1p5b_w16_zero1", None, None), ("zero3_24x50m_w8", None, None),
         ("gpt2_small_124m_w8_zero2", "bf16", None), ("gpt2_small_124m_w8_zero2", "fp16", None),
-        ("gpt2_small_124m_w8_zero2", "bf16", 1 << 24))
+        ("gpt2_small_124m_w8_zero2", "bf16", 1 << 24), ("gpt2_small_124m_w8_dp_replicas", "bf16", None),
+        ("gpt2_small_124m_w8_zero2_offload", "bf16", None))
 
 
 def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elems=None):
@@ -637,12 +639,20 @@ def run_ours(args):
             dt = dt or other.dtypes[0]
             if other.name == wl.name and dt == dtype and bucket is None:
                 continue
-            o_step, _, _, o_leg = device_leg(args, other, dt, dev, world, clocks_too=True, bucket_elems=bucket)
-            o_step.close()
+            if other.dp_replicas:
+                o_step, o_grads, _, _, o_leg = replicas_leg(args, other, dt, dev, world)
+                del o_grads
+            elif other.offload:
+                o_step, o_grads, _, _, o_leg = offload_leg(args, other, dt, dev, world)
+                del o_grads
+            else:
+                o_step, _, _, o_leg = device_leg(args, other, dt, dev, world, clocks_too=True, bucket_elems=bucket)
+            if hasattr(o_step, "close"):        # the replicas hold only tensors
+                o_step.close()
             del o_step
             torch.cuda.empty_cache()
             o_leg["config"] = config_of(other, dt, world)
-            key = f"{name}_{dt}" if name.startswith("gpt2_small") else name
+            key = f"{name}_{dt}" if name == "gpt2_small_124m_w8_zero2" else name
             if bucket:
                 key += f"_buckets_of_2p{bucket.bit_length() - 1}"
             also[key] = o_leg
@@ -908,12 +918,13 @@ def e2e_through_torch_copies(args, world, wl, su, grads, result, run_step, t0, p
     return e2e, t
 
 
-def run_replicas(args, wl, dtype, world, rank, dev):
+def replicas_leg(args, wl, dtype, dev, world):
     """Plain data parallelism with the W replicas kept literally
-    (zero_step_dp_replicas): every rank's fp32 master, m, v and 16-bit copy
-    in HBM, one kernel per step that reads the W gradients once and updates
-    all W replicas.  The same line as the sharded workloads, for the cost
-    that sharding removes."""
+    (zero_step_dp_replicas), its inputs resident in HBM: warm-up, then
+    ``args.steps`` timed steps, one kernel per step, and the bitwise check
+    that the replicas stayed equal.  Returns (the DpReplicas, the gradient
+    buffers, the update stream, the step counter reached, the leg's
+    figures)."""
     import torch
     import torch.distributed as dist
     import zero_sharded_mixed_step_gb300 as zs
@@ -966,7 +977,25 @@ def run_replicas(args, wl, dtype, world, rank, dev):
                 "kernel": "dp_replicas_step", "peak_source": f"{peak_src} copy bandwidth",
                 "launch_ms": ms_per_step, "algorithmic_bytes_per_launch": step_bytes,
                 "bytes_per_element": per_elem, "frac_of_8tbs_nominal": achieved / 8000.0, "launches_timed": launches}
+    resident = sum(x.numel() * x.element_size() for x in rep.master + rep.m + rep.v + rep.p16)
+    leg = {"workload": wl.name, "grad_dtype": dtype, "value": value, "unit": "params/s", "ms_per_step": ms_per_step,
+           "steps": args.steps, "warmup": args.warmup, "step_hbm_gbs": achieved, "step_frac_of_peak": achieved / peak,
+           "algorithmic_bytes_per_step": step_bytes, "replicated_state_bytes": resident, "roofline": roofline,
+           "gather": None, "gpu_launches": launches, "clocks": clocks.summary(), "replica_mismatches": 0}
+    return rep, grads, su, t, leg
 
+
+def run_replicas(args, wl, dtype, world, rank, dev):
+    """Plain data parallelism with the W replicas kept literally
+    (zero_step_dp_replicas): every rank's fp32 master, m, v and 16-bit copy
+    in HBM, one kernel per step that reads the W gradients once and updates
+    all W replicas.  The same line as the sharded workloads, for the cost
+    that sharding removes."""
+    import torch
+    import torch.distributed as dist
+
+    rep, grads, su, t, leg = replicas_leg(args, wl, dtype, dev, world)
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
         e2e, t = e2e_through_torch_copies(
@@ -974,21 +1003,20 @@ def run_replicas(args, wl, dtype, world, rank, dev):
             "host gradients (zero_host_alloc) -> device gradient buffers (one copy per rank) -> "
             "zero_step_dp_replicas -> replica 0's 16-bit working copy -> host, one stream")
 
-    resident = sum(x.numel() * x.element_size() for x in rep.master + rep.m + rep.v + rep.p16)
     del rep, grads
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, dtype, args.cpu_seconds)
     if rank == 0:
         config = config_of(wl, dtype, world)
-        config["replicated_state_bytes"] = resident
+        config["replicated_state_bytes"] = leg["replicated_state_bytes"]
         line = {
-            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "metric": METRIC, "value": leg["value"], "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": leg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
-            "step_hbm_gbs": achieved, "step_frac_of_peak": achieved / peak,
-            "roofline": roofline, "gather": None, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks.summary(),
+            "step_hbm_gbs": leg["step_hbm_gbs"], "step_frac_of_peak": leg["step_frac_of_peak"],
+            "roofline": leg["roofline"], "gather": None, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": leg["gpu_launches"], "clocks": leg["clocks"],
         }
         print(json.dumps(line))
     if world > 1:
@@ -1016,11 +1044,12 @@ def host_copy_gbs(threads: int, nbytes: int = 1 << 31) -> float:
         torch.set_num_threads(old)
 
 
-def run_offload(args, wl, dtype, world, rank, dev):
-    """ZeRO-2 with the optimizer on the host (zero_offload_step): the GPU forms
-    the mean gradient, host threads run Adam on host-resident fp32 state, the
-    16-bit copy streams back.  Same line as the other workloads; the roofline
-    is that of the host update, which bounds the step."""
+def offload_leg(args, wl, dtype, dev, world):
+    """ZeRO-2 with the optimizer on the host (zero_offload_step), its
+    gradients resident in HBM: warm-up, then ``args.steps`` timed steps; the
+    roofline is that of the host update, which bounds the step.  Returns (the
+    ZeroOffload, the gradient buffers, the update stream, the step counter
+    reached, the leg's figures)."""
     import torch
     import torch.distributed as dist
     import zero_sharded_mixed_step_gb300 as zs
@@ -1073,7 +1102,23 @@ def run_offload(args, wl, dtype, world, rank, dev):
     launches = st1["launches"] - st0["launches"]
     link = {"d2h_bytes_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) // args.steps,
             "h2d_bytes_per_step": (st1["h2d_bytes"] - st0["h2d_bytes"]) // args.steps}
+    leg = {"workload": wl.name, "grad_dtype": dtype, "value": value, "unit": "params/s", "ms_per_step": ms_per_step,
+           "steps": args.steps, "warmup": args.warmup,
+           "algorithmic_bytes_per_step": (2 * wl.W + 4) * off.n_pad + host_bytes, "offload_link_bytes_per_step": link,
+           "roofline": roofline, "gather": None, "gpu_launches": launches, "clocks": clocks.summary()}
+    return off, grads, su, t, leg
 
+
+def run_offload(args, wl, dtype, world, rank, dev):
+    """ZeRO-2 with the optimizer on the host (zero_offload_step): the GPU forms
+    the mean gradient, host threads run Adam on host-resident fp32 state, the
+    16-bit copy streams back.  Same line as the other workloads; the roofline
+    is that of the host update, which bounds the step."""
+    import torch
+    import torch.distributed as dist
+
+    off, grads, su, t, leg = offload_leg(args, wl, dtype, dev, world)
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
         e2e, t = e2e_through_torch_copies(
@@ -1088,14 +1133,14 @@ def run_offload(args, wl, dtype, world, rank, dev):
         cpu = cpu_baseline(wl, dtype, args.cpu_seconds)
     if rank == 0:
         config = config_of(wl, dtype, world)
-        config["algorithmic_bytes_per_step"] = (2 * wl.W + 4) * off.n_pad + host_bytes
-        config["offload_link_bytes_per_step"] = link
+        config["algorithmic_bytes_per_step"] = leg["algorithmic_bytes_per_step"]
+        config["offload_link_bytes_per_step"] = leg["offload_link_bytes_per_step"]
         line = {
-            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "metric": METRIC, "value": leg["value"], "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": leg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
-            "roofline": roofline, "gather": None, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks.summary(),
+            "roofline": leg["roofline"], "gather": None, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": leg["gpu_launches"], "clocks": leg["clocks"],
         }
         print(json.dumps(line))
     if world > 1:
