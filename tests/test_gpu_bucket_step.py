@@ -93,3 +93,58 @@ def test_bucketed_step_coverage_rules():
     s.sync()
     assert s.stat(zs.ZERO_STAT_T) == 2
     s.close()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_bucketed_configurations(seed):
+    """Seeded random configurations of the bucketed step: scheme (DP, ZeRO-1,
+    ZeRO-2), W from 1 to 64, both 16-bit formats, a ragged n, buckets from 8
+    values to the whole vector in shuffled order, a variant of the fused
+    pass, and each bucket's gradients in a buffer of its own at any 16-byte
+    aligned address.  Bit for bit against zero_step, every position against
+    the oracle, three steps."""
+    rng = np.random.default_rng(4000 + seed)
+    scheme = int(rng.integers(0, 3))
+    W = int(rng.choice([1, 2, 3, 5, 8, 16, 31, 64]))
+    max_len = int(rng.choice([64, 4096, 100_000, 1 << 40]))         # 2^40: one bucket for the whole vector
+    n = int(rng.integers(1, 600_000 if max_len > 64 else 30_000))    # tiny buckets only on short vectors
+    gdt, wdt = (str(rng.choice(["fp16", "bf16"])) for _ in range(2))
+    variant = int(rng.choice([zs.ZERO_VARIANT_AUTO, zs.ZERO_VARIANT_VECTOR, zs.ZERO_VARIANT_BULK]))
+    what = f"seed {seed}: scheme {scheme}, W {W}, n {n}, {gdt}->{wdt}, variant {variant}"
+    wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=3, name=f"bucket_random{seed}")
+    theta0 = wk.draw_theta0(wl, "cuda")
+    a = zs.ZeroStep(scheme, W, [n], gdt, wdt, theta0=theta0)
+    b = zs.ZeroStep(scheme, W, [n], gdt, wdt, theta0=theta0)
+    a.set_variant(variant)
+    b.set_variant(variant)
+    oracle = z.SingleReplica(theta0.cpu().numpy(), wdt, grad_dtype=gdt)
+    src = wk.GradSource(wl, gdt, "cuda")
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    for t in range(1, wl.steps + 1):
+        full = []
+        for d in src.step(t):
+            g = torch.zeros(a.n_pad, dtype=a.grad_torch_dtype, device="cuda")
+            a.place_(g, d)
+            full.append(g)
+        a.step(full, *hp, t)
+        for lo, hi in buckets_of(b.n_pad, rng, max_len=min(max_len, b.n_pad + 8)):
+            # each bucket in a buffer of its own, at an odd multiple of 16 bytes
+            bucket = []
+            for g in full:
+                room = torch.empty(hi - lo + 8, dtype=g.dtype, device="cuda")
+                view = room[8:] if room.data_ptr() % 32 == 0 else room[:hi - lo]
+                view.copy_(g[lo:hi])
+                bucket.append(view)
+            zs.zero_step_bucket(b.ctx, lo, hi - lo, bucket, *hp, t)
+        oracle.step([wk.to_numpy16(g[:n]) for g in full], *hp)
+        torch.cuda.synchronize()
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), (what, t)
+        assert torch.equal(a.p16.view(torch.int16), b.p16.view(torch.int16)), (what, t)
+        gh.assert_f32_parity(b.master[:n].cpu().numpy(), oracle.master, f"{what} t={t} master")
+        gh.assert_f32_parity(b.m[:n].cpu().numpy(), oracle.m, f"{what} t={t} m")
+        gh.assert_f32_parity(b.v[:n].cpu().numpy(), oracle.v, f"{what} t={t} v")
+        gh.assert_16bit_band(gh.bits_of(b.p16[:n]), oracle.master, wdt, f"{what} t={t}")
+    assert zs.zero_comm_bytes_per_rank(b.ctx) == zs.zero_comm_bytes_per_rank(a.ctx), what
+    a.close()
+    b.close()

@@ -214,3 +214,28 @@ def test_host_step_with_the_headline_chunking():
     block.close()
     a.close()
     b.close()
+
+
+def _random_case(seed):
+    """A seeded random case of test_host_step_equals_device_step's form."""
+    import numpy as np
+    rng = np.random.default_rng(6000 + seed)
+    scheme = int(rng.integers(0, 4))
+    W = int(rng.choice([1, 2, 3, 5, 8, 16, 24]))
+    if scheme == zs.ZERO_SCHEME_Z3:
+        size = [int(rng.choice([0, 1, 7, 4096, int(rng.integers(10, 400_000))])) for _ in range(int(rng.integers(1, 6)))]
+        if sum(size) == 0:
+            size[0] = 1
+    else:
+        size = int(rng.integers(1, 1_500_000))
+    chunk = int(rng.choice([0, 1000, 65_536, int(rng.integers(8, 300_000))]))
+    mem = str(rng.choice(["pin", "page", "huge"]))
+    return (scheme, size, W, str(rng.choice(["fp16", "bf16"])), chunk, mem, bool(rng.random() < 0.8))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_host_fed_configurations(seed):
+    """Seeded random schemes, rank counts, sizes (ZeRO-3: ragged and empty
+    units), chunk lengths, kinds of host memory and read-back: the host-fed
+    step bit for bit equal to the device step, three steps each."""
+    test_host_step_equals_device_step(_random_case(seed))
