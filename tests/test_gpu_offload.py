@@ -143,3 +143,42 @@ def test_offloaded_step_resumes_from_a_checkpoint():
         b.set_step(-1)
     a.close()
     b.close()
+
+
+def _random_case(seed):
+    import numpy as np
+    rng = np.random.default_rng(8000 + seed)
+    W = int(rng.choice([1, 2, 3, 5, 8, 16, 31, 64]))
+    n = int(rng.integers(1, 1_200_000 if W <= 16 else 200_000))
+    gdt, wdt = (str(rng.choice([wk.FP16, wk.BF16])) for _ in range(2))
+    chunk = int(rng.choice([0, 8, 4096, int(rng.integers(8, 500_000))]))
+    if chunk and n // chunk > 2000:                  # keep the number of chunks per step modest
+        chunk = 0
+    return n, W, gdt, wdt, chunk, int(rng.integers(1, 9))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_offloaded_configurations(seed):
+    """Seeded random rank counts (1 to 64), sizes, 16-bit formats, chunk
+    lengths and host thread counts: the offloaded step bit for bit equal to
+    the device step, three steps each."""
+    n, W, gdt, wdt, chunk, threads = _random_case(seed)
+    what = f"seed {seed}: n {n}, W {W}, {gdt}->{wdt}, chunk {chunk}, threads {threads}"
+    wl = wk.scaled(wk.GPT2_SMALL, n=n, W=W, steps=3, name=f"offload_random{seed}")
+    theta0 = wk.draw_theta0(wl, "cuda")
+    dev = zs.ZeroStep(zs.ZERO_SCHEME_Z2, W, [n], gdt, wdt, theta0=theta0)
+    off = zs.ZeroOffload(W, n, gdt, wdt, theta0=theta0.cpu(), chunk_elems=chunk, threads=threads)
+    src = wk.GradSource(wl, gdt, "cuda")
+    grads = dev.new_grad_buffers()
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    for t in range(1, wl.steps + 1):
+        for g, d in zip(grads, src.step(t)):
+            g[:n].copy_(d)
+        dev.step(grads, *hp, t)
+        off.step(grads, *hp, t)
+        torch.cuda.synchronize()
+        for mine, theirs in ((off.master, dev.master), (off.m, dev.m), (off.v, dev.v)):
+            assert _equal(mine, theirs.cpu()), (what, t)
+        assert _equal(off.p16, dev.p16), (what, t)
+    off.close()
+    dev.close()
