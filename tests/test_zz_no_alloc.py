@@ -158,3 +158,46 @@ def test_static_scratch_step_survives_a_device_reset(tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert run.returncode == 0, run.stdout + run.stderr
     assert "before and after cudaDeviceReset" in run.stdout
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_static_scratch_random_configurations(seed):
+    """Seeded random rank counts (1 to 64), units (empty, ragged, up to the
+    array's limit once padded), 16-bit formats, with and without a hook: two
+    calls in a row equal to zero_step's state bit for bit."""
+    rng = np.random.default_rng(3000 + seed)
+    Wr = int(rng.choice([1, 2, 3, 5, 8, 16, 31, 64]))
+    limit = 8_388_608 // Wr * Wr                       # the largest padded unit the array holds
+    units = [int(rng.choice([0, 1, 17, int(rng.integers(2, 200_000)), limit - int(rng.integers(0, Wr))]))
+             for _ in range(int(rng.integers(1, 5)))]
+    if sum(units) == 0:
+        units[0] = 5
+    gdt, wdt = (str(rng.choice(["fp16", "bf16"])) for _ in range(2))
+    with_hook = bool(rng.random() < 0.5)
+    what = f"seed {seed}: W {Wr}, units {units}, {gdt}->{wdt}, hook {with_hook}"
+    wl = wk.scaled(wk.LAYER_UNITS, W=Wr, unit_sizes=units, steps=2, name=f"static_random{seed}")
+    ref = zs.ZeroStep(zs.ZERO_SCHEME_Z3, Wr, units, gdt, wdt, theta0=wk.draw_theta0(wl, "cuda"))
+    master, m, v = ref.master.clone(), torch.zeros_like(ref.m), torch.zeros_like(ref.v)
+    shards = [s.clone() for s in ref.shard16]
+    calls = []
+    src = wk.GradSource(wl, gdt, "cuda")
+    hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
+    G = {"fp16": zs.ZERO_FP16, "bf16": zs.ZERO_BF16}
+    for t in (1, 2):
+        grads = ref.new_grad_buffers()
+        for g, d in zip(grads, src.step(t)):
+            ref.place_(g, d)
+        torch.cuda.synchronize()
+        ref.step(grads, *hp, t)
+        zs.zero_step_z3_static(Wr, units, G[gdt], G[wdt], master, m, v, shards, grads, *hp, t,
+                               hook=(lambda _u, ph, un, _b, _s: calls.append((ph, un))) if with_hook else None)
+        torch.cuda.synchronize()
+        for mine, theirs, name in ((master, ref.master, "master"), (m, ref.m, "m"), (v, ref.v, "v")):
+            assert torch.equal(mine.view(torch.int32), theirs.view(torch.int32)), (what, t, name)
+        for r in range(Wr):
+            assert torch.equal(shards[r].view(torch.int16), ref.shard16[r].view(torch.int16)), (what, t, r)
+    U = len(units)
+    if with_hook:
+        order = [(0, u) for u in range(U)] + [(1, u) for u in reversed(range(U))]
+        assert calls == order * 2, what
+    ref.close()
