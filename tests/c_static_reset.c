@@ -2,14 +2,14 @@
  * The ZeRO-3 step that allocates nothing (zero_step_z3_static), across a
  * device reset, from plain C.
  *
- * Round 1 runs one ZeRO-3 step twice on the same inputs: through a context
+ * Pass 1 runs one ZeRO-3 step twice on the same inputs: through a context
  * (zero_step, with its two caller-allocated unit buffers) and through
  * zero_step_z3_static (gathering into the library's own device array), and
  * requires the same bits.  Then cudaDeviceReset tears the device's context
  * down - every allocation is freed and the library's device code, with the
- * array, is unloaded - and round 2 allocates everything again, restores
- * round 1's state and runs step 2 the same two ways.  The array's device
- * address is looked up on every call, so round 2 finds it wherever the
+ * array, is unloaded - and pass 2 allocates everything again, restores
+ * pass 1's state and runs step 2 the same two ways.  The array's device
+ * address is looked up on every call, so pass 2 finds it wherever the
  * reloaded module put it.  This program and the library must share one CUDA
  * runtime (both link the shared libcudart).  Exit status 0 on success.
  */
@@ -68,8 +68,8 @@ int main(void) {
   uint64_t state = 99;
   const double lr = 3e-4, b1 = 0.9, b2 = 0.95, eps = 1e-8;
 
-  for (int round = 1; round <= 2; ++round) {
-    const int64_t t = round;
+  for (int pass = 1; pass <= 2; ++pass) {
+    const int64_t t = pass;
     float *master, *m, *v, *sm, *smm, *sv;
     void *shard[W], *sshard[W], *grads[W], *ub[2];
     CUDA(cudaMalloc((void**)&master, n_pad * 4));
@@ -116,28 +116,28 @@ int main(void) {
     CHECK(zero_sync(ctx, 60000) == ZERO_OK, "sync: %s", zero_last_error());
     hook_calls = 0;
     CHECK(zero_step_z3_static(W, U, units, ZERO_BF16, ZERO_BF16, sm, smm, sv, sshard, (const void* const*)grads, lr,
-                              b1, b2, eps, t, round == 2 ? count_hook : NULL, NULL, NULL) == ZERO_OK,
-          "static step (round %d): %s", round, zero_last_error());
+                              b1, b2, eps, t, pass == 2 ? count_hook : NULL, NULL, NULL) == ZERO_OK,
+          "static step (pass %d): %s", pass, zero_last_error());
     CUDA(cudaDeviceSynchronize());
-    CHECK(round == 1 || hook_calls == 2 * U, "hook ran %d times", hook_calls);
+    CHECK(pass == 1 || hook_calls == 2 * U, "hook ran %d times", hook_calls);
 
     float* pairs[3][2] = {{master, sm}, {m, smm}, {v, sv}};
     float* keep[3] = {h_master, h_m, h_v};
     for (int k = 0; k < 3; ++k) {
       CUDA(cudaMemcpy(keep[k], pairs[k][0], n_pad * 4, cudaMemcpyDeviceToHost));
       CUDA(cudaMemcpy(got, pairs[k][1], n_pad * 4, cudaMemcpyDeviceToHost));
-      CHECK(memcmp(got, keep[k], (size_t)n_pad * 4) == 0, "round %d: state %d differs from zero_step's", round, k);
+      CHECK(memcmp(got, keep[k], (size_t)n_pad * 4) == 0, "pass %d: state %d differs from zero_step's", pass, k);
     }
     for (int r = 0; r < W; ++r) {
       CUDA(cudaMemcpy(h16a, shard[r], s16 * 2, cudaMemcpyDeviceToHost));
       CUDA(cudaMemcpy(h16b, sshard[r], s16 * 2, cudaMemcpyDeviceToHost));
-      CHECK(memcmp(h16a, h16b, (size_t)s16 * 2) == 0, "round %d: shard store %d differs", round, r);
+      CHECK(memcmp(h16a, h16b, (size_t)s16 * 2) == 0, "pass %d: shard store %d differs", pass, r);
     }
     int moved = 0;
     for (int64_t i = 0; i < n_pad; ++i) moved += h_m[i] != 0.0f;
-    CHECK(moved > n / 2, "round %d: the step moved almost nothing (%d)", round, moved);
+    CHECK(moved > n / 2, "pass %d: the step moved almost nothing (%d)", pass, moved);
     CHECK(zero_destroy(ctx) == ZERO_OK, "destroy: %s", zero_last_error());
-    if (round == 1) {
+    if (pass == 1) {
       /* frees every allocation above and unloads the library's device code */
       CUDA(cudaDeviceReset());
     }
