@@ -69,6 +69,11 @@ def parse_args(argv=None):
     p.add_argument("--units", type=int, default=None,
                    help="ZeRO-3 only: keep the first N units (a smaller copy of the workload with the same "
                         "per-unit launches, for profiling)")
+    p.add_argument("--variant", choices=["auto", "vector", "bulk"], default="auto",
+                   help="the fused kernel the headline workload runs (zero_set_variant; for profiling)")
+    p.add_argument("--hook", action="store_true",
+                   help="ZeRO-3 headline: register an empty unit hook, so the step runs its prefetch schedule "
+                        "(a gather launch per unit on the gather stream; for profiling)")
     p.add_argument("--no-also", action="store_true",
                    help="time only the headline workload (not the other configurations under 'also')")
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -405,7 +410,8 @@ ALSO = (("gpt2_1p5b_w16_zero1", None, None), ("zero3_24x50m_w8", None, None),
         ("gpt2_small_124m_w8_zero2_offload", "bf16", None))
 
 
-def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elems=None):
+def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elems=None, variant="auto",
+               hook=False):
     """The step with its inputs resident in HBM: warm-up, then ``args.steps``
     timed steps (pass 1, CUDA events around the loop on the update stream),
     then the same steps again with a CUDA event pair around every launch
@@ -429,7 +435,11 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elem
         theta0 = wk.draw_theta0(wl, dev)
         step = zs.ZeroStep(scheme, wl.W, units, dtype, theta0=theta0, device=dev, stream=su, gather_stream=sg,
                            with_grad_buffers=True)
-        if scheme == 3:
+        step.set_variant({"auto": zs.ZERO_VARIANT_AUTO, "vector": zs.ZERO_VARIANT_VECTOR,
+                          "bulk": zs.ZERO_VARIANT_BULK}[variant])
+        if scheme == 3 and hook:
+            step.set_unit_hook(lambda user, phase, unit, buf, stream: None)
+        elif scheme == 3:
             step.set_graph(True)     # the step's launches replayed from one captured graph
         del theta0
         for r, d in enumerate(wk.GradSource(wl, dtype, dev).step(1)):
@@ -498,7 +508,7 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elem
     # unit hook a ZeRO-3 update launch also performs its unit's backward
     # gather (2 bytes read + 2 written per element on top of 2 W + 26).
     peak, peak_src = hbm_peak()
-    per_elem = 2 * wl.W + 26 + (4 if scheme == 3 else 0)
+    per_elem = 2 * wl.W + 26 + (4 if scheme == 3 and not hook else 0)   # with a hook the gathers are separate
     per_launch_bytes = per_elem * (per_launch[0] if buckets is None else n_pad // len(buckets))
     fused_avg_ms = fused_ms / max(1, fused_n)
     achieved = per_launch_bytes / (fused_avg_ms / 1e3) / 1e9
@@ -513,10 +523,11 @@ def device_leg(args, wl, dtype, dev, world, clocks_too: bool = True, bucket_elem
     if gather_n:
         # the forward gathers move 2 bytes in and 2 out per element of every unit
         # (all units in one launch when they have one size, else two per launch;
-        # the backward gathers are inside the fused pass)
-        gather_bytes = 4 * n_pad * args.steps
+        # the backward gathers are inside the fused pass); with a hook every
+        # gather, forward and backward, is a launch of its own, one unit each
+        gather_bytes = (8 if hook else 4) * n_pad * args.steps
         achieved_g = gather_bytes / (gather_ms / 1e3) / 1e9
-        kernel = gather_kernel(wl)
+        kernel = "copy_segments" if hook else gather_kernel(wl)
         gather_info = {"kernel": kernel, "launch_ms": gather_ms / gather_n, "achieved_gbs": achieved_g,
                        "frac": achieved_g / peak, "launches": gather_n,
                        "bytes_per_launch": gather_bytes // gather_n,
@@ -555,7 +566,7 @@ def run_ours(args):
         return run_offload(args, wl, dtype, world, rank, dev)
     scheme = scheme_of(wl)
     n_pad, per_launch, units = layout_sizes(wl)
-    step, su, t, leg = device_leg(args, wl, dtype, dev, world)
+    step, su, t, leg = device_leg(args, wl, dtype, dev, world, variant=args.variant, hook=args.hook)
     hp = (wl.lr, wl.beta1, wl.beta2, wl.eps)
 
     # ---- end to end: gradients from page-locked host memory, working copy read back --

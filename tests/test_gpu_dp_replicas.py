@@ -147,3 +147,35 @@ def test_replicas_beyond_device_memory_are_refused_before_allocating():
     with pytest.raises(MemoryError, match="replicas"):
         zs.DpReplicas(16, wk.GPT2_XL.n, wk.FP16, device="cuda")
     assert torch.cuda.memory_allocated() == before
+
+
+def test_mismatch_counter_with_replicas_off_the_vector_grain():
+    """zero_dp_replicas_mismatches accepts buffers aligned only to their
+    element size; replicas one element off a 32-byte boundary take the
+    element-at-a-time path and count the same pairs as aligned ones."""
+    W, n = 3, 10_001
+    n_pad = -(-n // W) * W                 # the compare reads n_pad values of every vector
+    base = [torch.zeros(n_pad + 1, dtype=torch.float32, device="cuda") for _ in range(3 * W)]
+    b16 = [torch.zeros(n_pad + 1, dtype=torch.int16, device="cuda") for _ in range(W)]
+    th, m, v = (base[k * W:(k + 1) * W] for k in range(3))
+    vals = torch.linspace(-1, 1, n_pad + 1, device="cuda")
+    for x in th + m + v:
+        x.copy_(vals)
+    for x in b16:
+        x.copy_(torch.arange(n_pad + 1, device="cuda", dtype=torch.int16))
+    views = [[x[1:] for x in grp] for grp in (th, m, v)] + [[x[1:] for x in b16]]   # 4 and 2 bytes off
+    count = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    def mismatches():
+        zs.zero_dp_replicas_mismatches(W, n, *views, count)
+        torch.cuda.synchronize()
+        return int(count.item())
+
+    assert mismatches() == 0
+    th[1][1 + 17] += 1.0                  # element 17 of replica 1
+    v[2][1 + 17] += 1.0                   # element 17 of replica 2
+    b16[2][1 + n_pad - 1] += 1            # the last (padding) element of replica 2
+    m[1][1 + 17] += 1.0                   # the same pair as the first
+    assert mismatches() == 3
+    th[0][1 + 5000] += 1.0                # replica 0 is the reference
+    assert mismatches() == 3 + W - 1

@@ -58,6 +58,7 @@ struct ReplicaArgs {
 
 struct CompareArgs {
   int W;
+  int vec;                        // every replica 32-byte (fp32) and 16-byte (16-bit) aligned
   int64_t n;
   const float* master[kMaxRanks];
   const float* m[kMaxRanks];
@@ -151,17 +152,51 @@ __global__ void __launch_bounds__(kThreads) dp_replicas_step(const __grid_consta
 
 // Counts the (replica r >= 1, element e) pairs where any of master, m, v or
 // the 16-bit copy of replica r differs bitwise from replica 0.
+// Groups of 8 elements per thread where every replica allows it (32-byte
+// loads of master, m and v, 16-byte loads of the 16-bit copy), the rest one
+// element at a time; each comparison is a bitwise XOR of the words, with no
+// early exit, so that all of a replica's loads are in flight together.
 __global__ void __launch_bounds__(kCompareThreads) dp_replicas_compare(const __grid_constant__ CompareArgs a) {
   unsigned long long local = 0;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < a.n; e += nthreads) {
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t done = 0;
+  if (a.vec) {
+    const int64_t groups = a.n >> 3;
+    for (int64_t g = tid; g < groups; g += nthreads) {
+      const int64_t i = g << 3;
+      float t0[8], m0[8], v0[8];
+      ld_32B(a.master[0] + i, t0);
+      ld_32B(a.m[0] + i, m0);
+      ld_32B(a.v[0] + i, v0);
+      const uint4 p0 = ld_16B(a.p16[0] + i);
+      for (int r = 1; r < a.W; ++r) {
+        float t[8], m[8], v[8];
+        ld_32B(a.master[r] + i, t);
+        ld_32B(a.m[r] + i, m);
+        ld_32B(a.v[r] + i, v);
+        const uint4 p = ld_16B(a.p16[r] + i);
+        const uint32_t pd[4] = {p.x ^ p0.x, p.y ^ p0.y, p.z ^ p0.z, p.w ^ p0.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t d = (__float_as_uint(t[k]) ^ __float_as_uint(t0[k])) |
+                             (__float_as_uint(m[k]) ^ __float_as_uint(m0[k])) |
+                             (__float_as_uint(v[k]) ^ __float_as_uint(v0[k])) |
+                             ((pd[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);   // element k's half of its word
+          local += d != 0u ? 1u : 0u;
+        }
+      }
+    }
+    done = groups << 3;
+  }
+  for (int64_t e = done + tid; e < a.n; e += nthreads) {
     const uint32_t t0 = __float_as_uint(a.master[0][e]), m0 = __float_as_uint(a.m[0][e]);
     const uint32_t v0 = __float_as_uint(a.v[0][e]);
-    const uint16_t p0 = a.p16[0][e];
+    const uint32_t p0 = a.p16[0][e];
     for (int r = 1; r < a.W; ++r) {
-      const bool differs = __float_as_uint(a.master[r][e]) != t0 || __float_as_uint(a.m[r][e]) != m0 ||
-                           __float_as_uint(a.v[r][e]) != v0 || a.p16[r][e] != p0;
-      local += differs ? 1u : 0u;
+      const uint32_t d = (__float_as_uint(a.master[r][e]) ^ t0) | (__float_as_uint(a.m[r][e]) ^ m0) |
+                         (__float_as_uint(a.v[r][e]) ^ v0) | (static_cast<uint32_t>(a.p16[r][e]) ^ p0);
+      local += d != 0u ? 1u : 0u;
     }
   }
 #pragma unroll
@@ -290,12 +325,20 @@ extern "C" int zero_dp_replicas_mismatches(int W, int64_t n, const float* const*
     a.v[r] = v[r];
     a.p16[r] = static_cast<const uint16_t*>(p16[r]);
   }
+  a.vec = 1;
+  for (int r = 0; work && r < W; ++r)
+    if (!aligned(master[r], 32) || !aligned(m[r], 32) || !aligned(v[r], 32) || !aligned(p16[r], 16)) a.vec = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err = cudaMemsetAsync(mismatches, 0, sizeof(int64_t), s);
   if (err != cudaSuccess) return fail(ZERO_E_CUDA, cudaGetErrorString(err));
   if (!work) return ZERO_OK;
-  const int64_t needed = (n_pad + kCompareThreads - 1) / kCompareThreads;
-  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(sm_count()) * 8, needed));
+  const int64_t per_thread = a.vec ? 8 : 1;
+  const int64_t needed = (n_pad / per_thread + kCompareThreads) / kCompareThreads;
+  int per_sm = 0;   // one resident wave
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dp_replicas_compare, kCompareThreads, 0);
+  if (err != cudaSuccess) return fail(ZERO_E_CUDA, cudaGetErrorString(err));
+  const int64_t blocks =
+      std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(sm_count()) * std::max(per_sm, 1), needed));
   dp_replicas_compare<<<static_cast<unsigned>(blocks), kCompareThreads, 0, s>>>(a);
   err = cudaGetLastError();
   return err == cudaSuccess ? ZERO_OK : fail(ZERO_E_CUDA, cudaGetErrorString(err));
